@@ -1,0 +1,449 @@
+"""Benchmark of one tree-verification step on GB300.
+
+A step is the whole hot path over one synthetic verify step of the
+Llama-3.1-8B shaped workload (batch 1, 32 layers of 32 query / 8 KV heads of
+128, 4096 context tokens in shuffled 16-token pages, a 60-node EAGLE-3 style
+tree, 128256-entry fp32 logits with a planted accepted path of length 4):
+
+  32 x sv_tree_attention (one per layer) + sv_greedy_accept + sv_kv_commit
+
+The step is captured once in a CUDA graph and replayed.  The metric is tree
+nodes verified per second per layer (nodes x layers / step time).  The
+attention kernel is also timed alone (a graph of the 32 attention launches)
+to give its achieved HBM bandwidth against the measured GB300 copy peak.
+
+``--impl reference`` times the CPU oracle (NumPy float64, the machine's host
+cores) on a bounded sample of the same workload and extrapolates to the same
+metric.  With torchrun (N > 1) every rank runs an independent replica (the
+path has no exchange between GPUs) and rank 0 prints the aggregate.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "tree-verify nodes/s per layer; attention HBM GB/s as % of GB300 peak (1 GPU)"
+UNIT = "nodes/s/layer"
+FALLBACK_HBM_GBS = 6800.0
+WORKLOADS = {
+    "llama8b_eagle": "Llama-3.1-8B shaped verify step: batch 1, 32 layers x (32 q / 8 kv heads, head_dim 128), "
+                     "context 4096 in shuffled 16-token pages, 60-node EAGLE-3 static tree (depth 7), "
+                     "fp32 logits 60x128256 with a planted accepted path of length 4",
+    "serving_mix": "Batched serving mix: 32 sequences, context U[1000,1600], 60-node trees, Llama-3.1-8B attention",
+    "long_partial": "60000-token context, 48-node tree, full KV",
+    "long_partial_pv": "60000-token context, 48-node tree, SpecPV partial list (64 sink + 32x64 retrieved + last 1024)",
+    "specblock": "SpecBlock trees (<=128 nodes, depth <=12), batch 16, 64 q / 8 kv heads, context 16384",
+}
+
+
+# ---------------------------------------------------------------------------- helpers
+
+def _dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate_max(value: float, world: int):
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+        self.dev = device_index
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev),
+                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- workload
+
+def build_case(name: str, seed_offset: int = 0):
+    from synth import make_case
+    if name == "llama8b_eagle":
+        return make_case("llama8b_eagle"), False
+    if name == "serving_mix":
+        return make_case("serving_mix"), False
+    if name == "long_partial":
+        return make_case("long_partial", with_partial=True), False
+    if name == "long_partial_pv":
+        return make_case("long_partial", with_partial=True), True
+    if name == "specblock":
+        return make_case("specblock"), False
+    raise ValueError(name)
+
+
+class GpuStep:
+    """Device-resident inputs and the library calls of one verify step."""
+
+    def __init__(self, case, partial: bool, dev: str):
+        import torch
+
+        from speculative_decoding_tree_sv_gb300 import binding
+        self.torch, self.binding, self.case, self.partial = torch, binding, case, partial
+        c = case
+        self.dev = dev
+
+        def bf(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+        def i32(a):
+            return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+        self.T, self.Hq, self.Hkv, self.D = c.total_nodes, c.num_q_heads, c.num_kv_heads, c.head_dim
+        self.layers = c.num_layers
+        self.q = bf(c.q)
+        self.tree_k = bf(c.tree_k)
+        self.tree_v = bf(c.tree_v)
+        self.k_cache = bf(c.k_cache)
+        self.v_cache = bf(c.v_cache)
+        self.block_table = i32(c.block_table)
+        self.ctx_lens = i32(c.ctx_lens)
+        self.cu_nodes = i32(c.cu_nodes)
+        self.parents = i32(c.parents)
+        self.tokens = i32(c.tokens)
+        self.logits = torch.from_numpy(c.logits).to(dev)
+        self.kv_pages = i32(c.kv_pages) if partial else None
+        self.cu_kv_pages = i32(c.cu_kv_pages) if partial else None
+        self.max_kv_pages = int(np.diff(c.cu_kv_pages).max()) if partial else 0
+        self.out = torch.empty((self.layers, self.T, self.Hq, self.D), dtype=torch.bfloat16, device=dev)
+        self.params = []
+        ws_bytes = 0
+        for l in range(self.layers):
+            p = binding.make_attn_params(
+                q=self.q[l], tree_k=self.tree_k[l], tree_v=self.tree_v[l], k_cache=self.k_cache[l],
+                v_cache=self.v_cache[l], block_table=self.block_table, ctx_lens=self.ctx_lens,
+                cu_nodes=self.cu_nodes, parents=self.parents, out=self.out[l], total_nodes=self.T,
+                max_nodes=c.max_nodes, kv_pages=self.kv_pages, cu_kv_pages=self.cu_kv_pages,
+                max_kv_pages=self.max_kv_pages)
+            ws_bytes = max(ws_bytes, binding.sv_tree_attention_workspace_size(p))
+            self.params.append(p)
+        self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+        for p in self.params:
+            p.workspace, p.workspace_bytes = self.ws.data_ptr(), ws_bytes
+        self.splits = self._splits(ws_bytes)
+        B = c.batch
+        self.am = torch.empty(self.T, dtype=torch.int32, device=dev)
+        self.alen = torch.empty(B, dtype=torch.int32, device=dev)
+        self.anodes = torch.empty((B, c.max_depth + 1), dtype=torch.int32, device=dev)
+        self.bonus = torch.empty(B, dtype=torch.int32, device=dev)
+        self.ws_acc = torch.zeros(binding.sv_greedy_accept_workspace_size(B, self.T), dtype=torch.uint8,
+                                  device=dev)
+        self.new_lens = torch.empty(B, dtype=torch.int32, device=dev)
+
+    def _splits(self, ws_bytes):
+        rows = self.T * self.Hq
+        per_split = rows * self.D * 4 + rows * 4
+        return max(1, round((ws_bytes - 256) / per_split)) if ws_bytes > 256 else 1
+
+    def launches_per_step(self):
+        per_attn = 2 if self.splits > 1 else 1
+        return self.layers * per_attn + 2
+
+    def attention_all_layers(self):
+        for p in self.params:
+            self.binding.sv_tree_attention(p)
+
+    def accept_and_commit(self):
+        c, b = self.case, self.binding
+        b.sv_greedy_accept(self.logits, c.vocab, self.tokens, self.parents, self.cu_nodes, c.batch, self.T,
+                           c.max_nodes, c.max_depth, self.am, self.alen, self.anodes, self.bonus, self.ws_acc)
+        b.sv_kv_commit(self.tree_k, self.tree_v, self.T * self.Hkv * self.D, self.k_cache, self.v_cache,
+                       c.num_pages * self.Hkv * c.page_size * self.D, self.layers, c.num_pages,
+                       self.block_table, c.max_pages_per_seq, self.ctx_lens, self.cu_nodes, self.anodes,
+                       self.alen, c.batch, c.max_depth, self.Hkv, self.D, c.page_size, self.new_lens, self.ws)
+
+    def step(self):
+        self.attention_all_layers()
+        self.accept_and_commit()
+
+
+def _time_graph(torch, fn, steps: int, warmup: int, world: int):
+    """Capture fn in a CUDA graph, warm up, time `steps` replays (events on the
+    capturing stream, synchronize + barrier on both sides, max over ranks)."""
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        fn()  # eager warm-up outside the graph
+    torch.cuda.current_stream().wait_stream(stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream()
+    e0.record(cur)
+    for _ in range(steps):
+        g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    return aggregate_max(ms, world), g
+
+
+# ---------------------------------------------------------------------------- CPU oracle leg
+
+def oracle_step_seconds(case, partial: bool, attn_layers: int = 1):
+    """Times the oracle on `attn_layers` layers of attention plus one
+    acceptance and one full commit; returns (seconds per full step, detail)."""
+    import oracle
+    t0 = time.perf_counter()
+    for l in range(attn_layers):
+        oracle.tree_verify_attention(
+            case.q[l], case.tree_k[l], case.tree_v[l], case.k_cache[l], case.v_cache[l], case.block_table,
+            case.ctx_lens, case.cu_nodes, case.parents, page_size=case.page_size,
+            kv_pages=case.kv_pages if partial else None, cu_kv_pages=case.cu_kv_pages if partial else None)
+    t_attn = (time.perf_counter() - t0) / attn_layers
+    t1 = time.perf_counter()
+    acc = oracle.greedy_accept(case.logits, case.tokens, case.parents, case.cu_nodes)
+    t_acc = time.perf_counter() - t1
+    t2 = time.perf_counter()
+    oracle.kv_commit(case.k_cache, case.v_cache, case.tree_k, case.tree_v, case.block_table, case.ctx_lens,
+                     case.cu_nodes, acc["accepted_nodes"], acc["accept_len"], case.page_size)
+    t_commit = time.perf_counter() - t2
+    step = t_attn * case.num_layers + t_acc + t_commit
+    return step, dict(attn_layer_s=t_attn, accept_s=t_acc, commit_s=t_commit)
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    world, rank, _ = _dist_env()
+    if rank != 0:
+        return 0
+    case, partial = build_case(args.config)
+    nodes = case.total_nodes * case.num_layers
+    for _ in range(args.warmup):
+        oracle_step_seconds(case, partial)
+    times = []
+    for _ in range(args.steps):
+        s, _detail = oracle_step_seconds(case, partial)
+        times.append(s)
+    step_s = statistics.mean(times)
+    value = nodes / step_s
+    sample = (f"each step: oracle attention on 1 of {case.num_layers} layers (x{case.num_layers}), "
+              f"acceptance over all {case.total_nodes}x{case.vocab} logits, commit of all layers")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOADS[args.config]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------- GPU leg
+
+def run_gpu(args):
+    import torch
+
+    from speculative_decoding_tree_sv_gb300 import build as _build
+    from speculative_decoding_tree_sv_gb300 import cost
+
+    world, rank, local = _dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    _build.build()
+    case, partial = build_case(args.config)
+    st = GpuStep(case, partial, dev)
+    c = case
+    nodes_per_step = c.total_nodes * c.num_layers
+
+    # whole step, graph-replayed, clocks sampled meanwhile
+    with ClockSampler(local) as clk:
+        ms, _g = _time_graph(torch, st.step, args.steps, args.warmup, world)
+        # attention alone (the dominant kernel) for the roofline
+        ms_attn, _ga = _time_graph(torch, st.attention_all_layers, args.steps, args.warmup, world)
+    clocks = clk.summary()
+    ms_step = ms / args.steps
+    value = world * nodes_per_step / (ms_step * 1e-3)
+
+    # algorithmic bytes of one attention launch
+    if partial:
+        ctx_keys = [cost.context_keys(int(c.ctx_lens[b]), c.page_size,
+                                      c.kv_pages[c.cu_kv_pages[b]:c.cu_kv_pages[b + 1]]) for b in range(c.batch)]
+    else:
+        ctx_keys = [int(x) for x in c.ctx_lens]
+    ns = np.diff(c.cu_nodes)
+    bytes_launch = cost.attention_bytes(ctx_keys, ns, c.num_q_heads, c.num_kv_heads, c.head_dim)
+    attn_launch_s = ms_attn * 1e-3 / (args.steps * c.num_layers)
+    achieved = bytes_launch / attn_launch_s / 1e9
+    peak, peak_kind = measured_peaks()
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", f"traffic_{args.config}.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            traffic = json.load(f).get("dram_bytes_per_launch")
+
+    # end to end through the public API with host buffers: pinned H2D of the
+    # step's inputs, the step, D2H of the results; captured like the step.
+    pin = {}
+    h2d = 0
+    for name in ("q", "tree_k", "tree_v", "logits", "parents", "tokens", "cu_nodes", "ctx_lens"):
+        t = getattr(st, name)
+        pin[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+        h2d += t.numel() * t.element_size()
+    res_host = {n: torch.empty(getattr(st, n).shape, dtype=torch.int32, pin_memory=True)
+                for n in ("alen", "anodes", "bonus")}
+    d2h = sum(v.numel() * 4 for v in res_host.values())
+
+    def e2e_step():
+        for name, h in pin.items():
+            getattr(st, name).copy_(h, non_blocking=True)
+        st.step()
+        for n, h in res_host.items():
+            h.copy_(getattr(st, n), non_blocking=True)
+
+    ms_e2e, _ge = _time_graph(torch, e2e_step, args.steps, args.warmup, world)
+    e2e_value = world * nodes_per_step / (ms_e2e * 1e-3 / args.steps)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        s, detail = oracle_step_seconds(case, partial)
+        cpu = {"value": nodes_per_step / s, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+               "sample": f"oracle (NumPy fp64) attention on 1 of {c.num_layers} layers scaled x{c.num_layers}, "
+                         f"acceptance over all {c.total_nodes}x{c.vocab} logits and the commit of all layers: "
+                         + ", ".join(f"{k} {v:.3f}" for k, v in detail.items())}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOADS[args.config], "layers": c.num_layers, "batch": c.batch,
+                       "total_nodes": c.total_nodes, "kv_splits": st.splits, "cuda_graph": True,
+                       "l2": "inputs larger than L2 (distinct KV per layer, %.0f MB per step)"
+                             % (sum(ctx_keys) * 4 * c.num_kv_heads * c.head_dim * c.num_layers / 1e6),
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+                         "kernel": "sv_tree_attention (attention + split combine)",
+                         "bytes_per_launch": bytes_launch, "launch_us": attn_launch_s * 1e6},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": st.launches_per_step() * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["sv", "reference"], default="sv")
+    ap.add_argument("--config", choices=sorted(WORKLOADS), default="llama8b_eagle")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

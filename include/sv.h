@@ -1,0 +1,214 @@
+/*
+ * sv.h — C ABI of the GB300 (sm_103a) tree-verification library (libsv.so).
+ *
+ * Speculative decoding drafts a tree of candidate tokens and has the target
+ * model score every node in one forward pass, then commits the longest
+ * accepted prefix (SpecBlock, Appendix A.5 "Inference procedure"; SpecPV,
+ * section 1 and section 3.2).  This library implements the data-parallel
+ * hot path of that verification step:
+ *
+ *   sv_tree_attention  tree-masked, paged GQA attention of all tree nodes
+ *                      against the context KV cache (full, or a SpecPV
+ *                      partial page list), one layer per call;
+ *   sv_greedy_accept   per-node vocabulary arg-max and the longest accepted
+ *                      root path (temperature 0);
+ *   sv_kv_commit       copy of the accepted path's K/V into the paged cache
+ *                      for every layer.
+ *
+ * Conventions shared by every entry point
+ *   - All pointers not marked "host" are device pointers.  The caller owns
+ *     all memory; the library allocates nothing.
+ *   - Every call is asynchronous on the given stream and performs no host
+ *     synchronisation (sv_get_device_error excepted).
+ *   - Host-checkable errors (null pointers, unsupported shapes, misaligned
+ *     pointers, workspace too small) return synchronously without launching
+ *     anything.  Launch failures return SV_ERR_CUDA.
+ *   - Device-resident index data (block tables, parents, page lists, paths)
+ *     is range-checked by the kernels: an out-of-range value is skipped and
+ *     recorded as a nonzero code in the workspace's error word, never as a
+ *     trap.  Read it with sv_get_device_error.
+ *   - bf16 tensors are IEEE bfloat16, little endian, rows contiguous, and
+ *     must start on 16-byte boundaries.  Inputs are finite; NaN is
+ *     unsupported.
+ *   - A workspace must be zero-filled once after allocation (for example with
+ *     cudaMemset) and must not be shared by calls that may run concurrently.
+ *     Each call leaves its workspace ready for the next call.
+ *   - Symbols are thread-safe; per-stream ordering is the caller's.
+ */
+#ifndef SV_H_
+#define SV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st* sv_stream_t;
+
+typedef enum sv_status {
+  SV_OK = 0,
+  SV_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer   */
+  SV_ERR_UNSUPPORTED = 2,  /* shape outside the supported set             */
+  SV_ERR_CUDA = 3,         /* a CUDA runtime/driver call or launch failed */
+  SV_ERR_WORKSPACE = 4,    /* workspace missing or too small              */
+  SV_ERR_DEVICE = 5,       /* the device error word holds a nonzero code  */
+  SV_ERR_TIMEOUT = 6       /* a bounded device-side wait ran out          */
+} sv_status;
+
+/* Codes a kernel writes into the workspace's error word (first 4 bytes). */
+enum {
+  SV_DEVERR_NONE = 0,
+  SV_DEVERR_TIMEOUT = 1,     /* a bounded wait in a kernel ran out          */
+  SV_DEVERR_BAD_PARENT = 2,  /* parent[i] not in [0, i) for a non-root node */
+  SV_DEVERR_BAD_PAGE = 3,    /* page id outside [0, num_pages) or table     */
+  SV_DEVERR_BAD_PATH = 4,    /* accepted path node outside its tree         */
+  SV_DEVERR_DEPTH = 5,       /* accepted depth exceeds max_depth            */
+  SV_DEVERR_BAD_TREE = 6     /* a tree has no nodes or more than max_nodes  */
+};
+
+/* Library ABI version (incremented on incompatible changes). */
+int sv_abi_version(void);
+
+/* Static, human-readable name of a status code. */
+const char* sv_status_string(sv_status status);
+
+/* ------------------------------------------------------------------------
+ * Tree-verification attention (one layer).
+ *
+ * Defined by: SpecBlock Appendix A.5 (all drafted positions scored in one
+ * parallel target forward); SpecBlock Appendix A.2 (a position sees the
+ * verified prefix and its on-path predecessors, off-path positions are
+ * masked); SpecPV section 3.2 (partial verification: the retained sink,
+ * retrieved, window and buffer blocks form one continuous KV segment).
+ *
+ * For sequence b with N_b tree nodes and context length L_b, node i of the
+ * tree (sequence-local index; node 0 is the root, the last accepted token)
+ * and query head h (KV head h / G, G = Hq / Hkv) computes
+ *     out[i,h] = sum_j softmax_j(scale * q[i,h] . k_j) v_j
+ * over the keys j = the context tokens (all of 0..L_b-1, or the tokens of
+ * the listed pages in list order) followed by the tree nodes that are
+ * ancestors of i or i itself.  The root is not part of L_b.  Q and K arrive
+ * with positional encoding already applied.
+ * ---------------------------------------------------------------------- */
+typedef struct sv_attn_params {
+  /* shapes (host values) */
+  int batch;              /* B >= 1                                          */
+  int num_q_heads;        /* Hq                                              */
+  int num_kv_heads;       /* Hkv; G = Hq / Hkv must be 1, 2, 4, 8 or 16     */
+  int head_dim;           /* D: 64 or 128                                    */
+  int page_size;          /* tokens per KV page: 16                          */
+  int num_pages;          /* pages in this layer's pool (cache dim 0)        */
+  int total_nodes;        /* T = cu_nodes[B] (host copy)                     */
+  int max_nodes;          /* max_b N_b (host copy), 1..128                   */
+  int max_pages_per_seq;  /* row length of block_table                       */
+  int max_kv_pages;       /* partial mode: max_b listed pages (host copy)    */
+  int num_splits;         /* KV splits per (sequence, head group); 0 = auto  */
+  float sm_scale;         /* softmax scale; <= 0 selects 1/sqrt(D)           */
+
+  /* tensors */
+  const void* q;          /* bf16 [T, Hq, D]                                 */
+  const void* tree_k;     /* bf16 [T, Hkv, D]  K of the tree nodes           */
+  const void* tree_v;     /* bf16 [T, Hkv, D]  V of the tree nodes           */
+  const void* k_cache;    /* bf16 [num_pages, Hkv, page_size, D]             */
+  const void* v_cache;    /* bf16 [num_pages, Hkv, page_size, D]             */
+  const int* block_table; /* int32 [B, max_pages_per_seq] logical->physical  */
+  const int* ctx_lens;    /* int32 [B] L_b >= 0                              */
+  const int* cu_nodes;    /* int32 [B+1] prefix sums of N_b, cu_nodes[0] = 0 */
+  const int* parents;     /* int32 [T] sequence-local parent, -1 at node 0,
+                             parent[i] < i otherwise                         */
+  const int* kv_pages;    /* optional int32 [sum] logical page ids per
+                             sequence, ascending and unique, each page <
+                             ceil(L_b / page_size); NULL = full verification */
+  const int* cu_kv_pages; /* int32 [B+1] prefix sums into kv_pages           */
+  void* out;              /* bf16 [T, Hq, D] (written)                       */
+  float* lse;             /* optional fp32 [T, Hq]: natural log of the
+                             softmax denominator (written if non-NULL)       */
+  void* workspace;        /* device scratch, see workspace_size              */
+  size_t workspace_bytes;
+} sv_attn_params;
+
+/* Bytes of workspace sv_tree_attention needs for these parameters (queries
+ * the current device's SM count when num_splits == 0). */
+sv_status sv_tree_attention_workspace_size(const sv_attn_params* params, size_t* bytes);
+
+/* Launches the attention (and, with more than one split, the split combine)
+ * on `stream`.  Grid: one CTA per (KV split, KV head x 256-row group,
+ * sequence); see the library's design notes for the kernel. */
+sv_status sv_tree_attention(const sv_attn_params* params, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Greedy acceptance (temperature 0).
+ *
+ * Defined by: SpecBlock Appendix A.5 (the longest accepted prefix is
+ * committed); greedy decoding at T = 0 (SpecBlock section 4, SpecPV
+ * Appendix D); the reported accept length excludes the bonus token
+ * ("Dynamic Speculative Decoding", Implementation Details: the scheduler
+ * keeps accept_length + 1 tokens per request).
+ *
+ * am[n] = argmax_v logits[n, v], lowest v on ties (-0.0 == +0.0).  Non-root
+ * node c is accepted iff tokens[c] == am[parent c] and its parent is
+ * accepted (the root always is).  The result per sequence is the deepest
+ * accepted node, ties broken by the lexicographically smallest root path of
+ * node indices:
+ *   accept_len[b]                 its depth (root and bonus excluded)
+ *   accepted_nodes[b, 0..a]       its root path (local ids, [0] = 0), the
+ *                                 remaining entries up to max_depth are -1
+ *   bonus_token[b]                am[last node of the path]
+ *   argmax_out[n]                 am[n] for every node (optional)
+ *
+ * logits: fp32 [T, vocab], rows contiguous.  tokens/parents: int32 [T]
+ * (tokens[root] unused).  max_nodes (host) <= 128.  max_depth (host) is the
+ * row stride - 1 of accepted_nodes and must be >= every tree's depth.
+ * ---------------------------------------------------------------------- */
+sv_status sv_greedy_accept_workspace_size(int batch, int total_nodes, size_t* bytes);
+
+sv_status sv_greedy_accept(const float* logits, int vocab, const int* tokens,
+                           const int* parents, const int* cu_nodes, int batch,
+                           int total_nodes, int max_nodes, int max_depth,
+                           int* argmax_out, int* accept_len, int* accepted_nodes,
+                           int* bonus_token, void* workspace, size_t workspace_bytes,
+                           sv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * KV commit of the accepted path, all layers in one launch.
+ *
+ * Defined by: SpecBlock Appendix A.5 (commit the accepted prefix before the
+ * next iteration) and "Dynamic Speculative Decoding", Implementation Details
+ * (the KV cache stays consistent with the committed tokens).
+ *
+ * For every layer l, sequence b and j = 0..accept_len[b]: cache slot
+ * s = ctx_lens[b] + j (page block_table[b, s / page_size], row
+ * s % page_size) receives, for every KV head, the K and V of tree node
+ * accepted_nodes[b, j] (a bit copy).  new_ctx_lens[b] = ctx_lens[b] +
+ * accept_len[b] + 1 if non-NULL; it must not alias ctx_lens.  The caller
+ * guarantees pages for slots L_b .. L_b + max_depth.  Nothing else changes.
+ *
+ * tree_k/tree_v: bf16 [num_layers][T, Hkv, D], layer stride
+ * tree_layer_stride elements.  k_cache/v_cache: bf16
+ * [num_layers][num_pages, Hkv, page_size, D], layer stride
+ * cache_layer_stride elements.  Both strides are multiples of 8.
+ * workspace is optional (NULL, or >= 256 bytes zero-filled once) and only
+ * receives the error word.
+ * ---------------------------------------------------------------------- */
+sv_status sv_kv_commit(const void* tree_k, const void* tree_v, long long tree_layer_stride,
+                       void* k_cache, void* v_cache, long long cache_layer_stride,
+                       int num_layers, int num_pages, const int* block_table,
+                       int max_pages_per_seq, const int* ctx_lens, const int* cu_nodes,
+                       const int* accepted_nodes, const int* accept_len, int batch,
+                       int max_depth, int num_kv_heads, int head_dim, int page_size,
+                       int* new_ctx_lens, void* workspace, size_t workspace_bytes,
+                       sv_stream_t stream);
+
+/* Reads the error word of a workspace (waits for `stream`), stores it in
+ * *code (host) and resets it to zero.  Returns SV_ERR_DEVICE if it was
+ * nonzero, SV_OK otherwise. */
+sv_status sv_get_device_error(void* workspace, int* code, sv_stream_t stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* SV_H_ */

@@ -1,0 +1,195 @@
+"""ctypes binding of ``libsv.so`` (argument marshalling only).
+
+The functions carry the names of the C entry points declared in
+``include/sv.h``.  Tensor arguments may be torch tensors (their
+``data_ptr()`` is passed) or raw integer device addresses; ``stream``
+defaults to torch's current CUDA stream.  Every step of the computation
+runs in the library's CUDA kernels: if the library is not built, loading
+fails with an error instead of falling back to anything else.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import c_float, c_int, c_longlong, c_size_t, c_void_p
+from typing import Optional
+
+from . import build as _build
+
+SV_OK = 0
+STATUS_NAMES = {0: "SV_OK", 1: "SV_ERR_INVALID_ARG", 2: "SV_ERR_UNSUPPORTED", 3: "SV_ERR_CUDA",
+                4: "SV_ERR_WORKSPACE", 5: "SV_ERR_DEVICE", 6: "SV_ERR_TIMEOUT"}
+DEVICE_ERRORS = {0: "none", 1: "timeout", 2: "bad parent", 3: "bad page", 4: "bad path", 5: "depth",
+                 6: "bad tree"}
+
+
+class SvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+class sv_attn_params(ctypes.Structure):
+    _fields_ = [
+        ("batch", c_int), ("num_q_heads", c_int), ("num_kv_heads", c_int), ("head_dim", c_int),
+        ("page_size", c_int), ("num_pages", c_int), ("total_nodes", c_int), ("max_nodes", c_int),
+        ("max_pages_per_seq", c_int), ("max_kv_pages", c_int), ("num_splits", c_int),
+        ("sm_scale", c_float),
+        ("q", c_void_p), ("tree_k", c_void_p), ("tree_v", c_void_p), ("k_cache", c_void_p),
+        ("v_cache", c_void_p), ("block_table", c_void_p), ("ctx_lens", c_void_p),
+        ("cu_nodes", c_void_p), ("parents", c_void_p), ("kv_pages", c_void_p),
+        ("cu_kv_pages", c_void_p), ("out", c_void_p), ("lse", c_void_p), ("workspace", c_void_p),
+        ("workspace_bytes", c_size_t),
+    ]
+
+
+_LIB = None
+
+
+def load(path: Optional[str] = None):
+    """Load the built library (raises if it is missing)."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    path = path or _build.library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libsv.so is not built ({path}); run __graft_entry__.build() or "
+                           "python -m speculative_decoding_tree_sv_gb300.build")
+    lib = ctypes.CDLL(path)
+    P = ctypes.POINTER
+    lib.sv_abi_version.restype = c_int
+    lib.sv_abi_version.argtypes = []
+    lib.sv_status_string.restype = ctypes.c_char_p
+    lib.sv_status_string.argtypes = [c_int]
+    lib.sv_tree_attention_workspace_size.restype = c_int
+    lib.sv_tree_attention_workspace_size.argtypes = [P(sv_attn_params), P(c_size_t)]
+    lib.sv_tree_attention.restype = c_int
+    lib.sv_tree_attention.argtypes = [P(sv_attn_params), c_void_p]
+    lib.sv_greedy_accept_workspace_size.restype = c_int
+    lib.sv_greedy_accept_workspace_size.argtypes = [c_int, c_int, P(c_size_t)]
+    lib.sv_greedy_accept.restype = c_int
+    lib.sv_greedy_accept.argtypes = [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+                                     c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
+    lib.sv_kv_commit.restype = c_int
+    lib.sv_kv_commit.argtypes = [c_void_p, c_void_p, c_longlong, c_void_p, c_void_p, c_longlong, c_int, c_int,
+                                 c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
+                                 c_int, c_int, c_void_p, c_void_p, c_size_t, c_void_p]
+    lib.sv_get_device_error.restype = c_int
+    lib.sv_get_device_error.argtypes = [c_void_p, P(c_int), c_void_p]
+    if path == _build.library_path():
+        _LIB = lib
+    return lib
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != SV_OK:
+        raise SvError(status, where)
+
+
+def sv_abi_version() -> int:
+    return load().sv_abi_version()
+
+
+def sv_status_string(status: int) -> str:
+    return load().sv_status_string(status).decode()
+
+
+def make_attn_params(*, q, tree_k, tree_v, k_cache, v_cache, block_table, ctx_lens, cu_nodes, parents,
+                     out, total_nodes: int, max_nodes: int, workspace=None, workspace_bytes: int = 0,
+                     kv_pages=None, cu_kv_pages=None, max_kv_pages: int = 0, lse=None,
+                     sm_scale: float = 0.0, num_splits: int = 0, page_size: int = 16, batch=None,
+                     num_q_heads=None, num_kv_heads=None, head_dim=None, num_pages=None,
+                     max_pages_per_seq=None) -> sv_attn_params:
+    """Fill an ``sv_attn_params``; shapes come from torch tensors unless given."""
+    p = sv_attn_params()
+    p.batch = batch if batch is not None else int(block_table.shape[0])
+    p.num_q_heads = num_q_heads if num_q_heads is not None else int(q.shape[1])
+    p.num_kv_heads = num_kv_heads if num_kv_heads is not None else int(tree_k.shape[1])
+    p.head_dim = head_dim if head_dim is not None else int(q.shape[2])
+    p.page_size = page_size
+    p.num_pages = num_pages if num_pages is not None else int(k_cache.shape[0])
+    p.total_nodes = int(total_nodes)
+    p.max_nodes = int(max_nodes)
+    p.max_pages_per_seq = max_pages_per_seq if max_pages_per_seq is not None else int(block_table.shape[1])
+    p.max_kv_pages = int(max_kv_pages)
+    p.num_splits = int(num_splits)
+    p.sm_scale = float(sm_scale)
+    p.q, p.tree_k, p.tree_v = _ptr(q), _ptr(tree_k), _ptr(tree_v)
+    p.k_cache, p.v_cache = _ptr(k_cache), _ptr(v_cache)
+    p.block_table, p.ctx_lens, p.cu_nodes, p.parents = _ptr(block_table), _ptr(ctx_lens), _ptr(cu_nodes), _ptr(parents)
+    p.kv_pages, p.cu_kv_pages = _ptr(kv_pages), _ptr(cu_kv_pages)
+    p.out, p.lse = _ptr(out), _ptr(lse)
+    p.workspace = _ptr(workspace)
+    p.workspace_bytes = int(workspace_bytes if workspace_bytes else
+                            (workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0))
+    return p
+
+
+def sv_tree_attention_workspace_size(params: sv_attn_params) -> int:
+    n = c_size_t(0)
+    _check(load().sv_tree_attention_workspace_size(ctypes.byref(params), ctypes.byref(n)),
+           "sv_tree_attention_workspace_size")
+    return int(n.value)
+
+
+def sv_tree_attention(params: sv_attn_params, stream=None) -> None:
+    _check(load().sv_tree_attention(ctypes.byref(params), _stream(stream)), "sv_tree_attention")
+
+
+def sv_greedy_accept_workspace_size(batch: int, total_nodes: int) -> int:
+    n = c_size_t(0)
+    _check(load().sv_greedy_accept_workspace_size(batch, total_nodes, ctypes.byref(n)),
+           "sv_greedy_accept_workspace_size")
+    return int(n.value)
+
+
+def sv_greedy_accept(logits, vocab: int, tokens, parents, cu_nodes, batch: int, total_nodes: int,
+                     max_nodes: int, max_depth: int, argmax_out, accept_len, accepted_nodes, bonus_token,
+                     workspace, workspace_bytes: Optional[int] = None, stream=None) -> None:
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(load().sv_greedy_accept(_ptr(logits), vocab, _ptr(tokens), _ptr(parents), _ptr(cu_nodes), batch,
+                                   total_nodes, max_nodes, max_depth, _ptr(argmax_out), _ptr(accept_len),
+                                   _ptr(accepted_nodes), _ptr(bonus_token), _ptr(workspace), workspace_bytes,
+                                   _stream(stream)), "sv_greedy_accept")
+
+
+def sv_kv_commit(tree_k, tree_v, tree_layer_stride: int, k_cache, v_cache, cache_layer_stride: int,
+                 num_layers: int, num_pages: int, block_table, max_pages_per_seq: int, ctx_lens, cu_nodes,
+                 accepted_nodes, accept_len, batch: int, max_depth: int, num_kv_heads: int, head_dim: int,
+                 page_size: int = 16, new_ctx_lens=None, workspace=None, workspace_bytes: int = 0,
+                 stream=None) -> None:
+    if workspace is not None and not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(load().sv_kv_commit(_ptr(tree_k), _ptr(tree_v), tree_layer_stride, _ptr(k_cache), _ptr(v_cache),
+                               cache_layer_stride, num_layers, num_pages, _ptr(block_table), max_pages_per_seq,
+                               _ptr(ctx_lens), _ptr(cu_nodes), _ptr(accepted_nodes), _ptr(accept_len), batch,
+                               max_depth, num_kv_heads, head_dim, page_size, _ptr(new_ctx_lens),
+                               _ptr(workspace), workspace_bytes, _stream(stream)), "sv_kv_commit")
+
+
+def sv_get_device_error(workspace, stream=None) -> int:
+    """Returns the workspace's device error code (0 = none) and clears it."""
+    code = c_int(0)
+    st = load().sv_get_device_error(_ptr(workspace), ctypes.byref(code), _stream(stream))
+    if st not in (SV_OK, 5, 6):
+        _check(st, "sv_get_device_error")
+    return int(code.value)

@@ -1,0 +1,36 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/sv.h"
+
+namespace sv {
+
+// Bounded device waits give up after this long (a healthy wait takes
+// microseconds).
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+// Every workspace starts with a 256-byte header; the error word is at 0.
+constexpr size_t kWorkspaceHeader = 256;
+
+constexpr int kMaxNodes = 128;   // ancestor bitmask width / acceptance walk
+constexpr int kMaxSplits = 64;
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Tensor-map encoding through the driver entry point (resolved at first use,
+// so the library loads on machines without a GPU driver).
+CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, cuuint32_t rank, void* base,
+                      const cuuint64_t* dims, const cuuint64_t* strides_bytes, const cuuint32_t* box,
+                      CUtensorMapSwizzle swizzle, CUtensorMapL2promotion l2);
+
+// Number of SMs of the current device (cached per device); -1 on failure.
+int device_sm_count();
+
+}  // namespace sv

@@ -1,0 +1,752 @@
+// Tree-verification attention for sm_103a.
+//
+// What it computes (SpecBlock Appendix A.5: every drafted node is scored in
+// one target forward; Appendix A.2: a node sees the verified prefix and its
+// on-path ancestors; SpecPV section 3.2: a partial cache of retained blocks is
+// attended as one continuous KV segment): for every tree node i and query
+// head h,  out[i,h] = softmax(scale * q[i,h] K^T + mask) V  over the context
+// keys followed by the tree keys, where the tree part of the mask keeps only
+// ancestors-or-self of i.
+//
+// Design (one CTA per (KV split, KV head x 256-row group, sequence)):
+//   * The M dimension of the contraction is (tree node x query head of the
+//     GQA group): rows r = node * G + g, two 128-row tiles per CTA.
+//   * Context K/V pages (16 tokens, head-major inside a page) are gathered
+//     with TMA, eight pages (128 keys) per tile, 128-byte swizzled, into a
+//     ring of smem stages.  The tree's own K/V form one extra tile.
+//   * tcgen05.mma computes S = Q K^T (both operands K-major in smem) into
+//     TMEM; softmax warps read S with tcgen05.ld (one row per thread), apply
+//     the mask and an online, lazily rescaled softmax in base 2, write P as
+//     bf16 back into the S columns, and tcgen05.mma accumulates O += P V
+//     (P from TMEM, V MN-major in smem).
+//   * Warp roles: warp 0 loads (TMA), warp 1 issues MMAs (one thread),
+//     warps 4-7 and 8-11 run the softmax of row tiles 0 and 1.  The MMA
+//     issue order S0 S1 | PV0 S0' | PV1 S1' ... keeps the tensor core busy
+//     while the two softmax groups alternate.
+//   * Splits of the KV range write (O / l, log2-sum-exp) partials that a
+//     second kernel merges; with one split the output is written directly.
+#include <math.h>
+
+#include <mutex>
+
+#include "sv_device.cuh"
+
+namespace sv {
+namespace attn {
+
+constexpr int kThreads = 384;
+// Registers per thread after the split: 128 x 56 (load + MMA group) + 256 x
+// 224 (softmax groups) = 64512 = 384 x 168, the launch allocation.
+constexpr int kRegsControl = 56;
+constexpr int kRegsSoftmax = 224;
+constexpr int kBlockN = 128;       // keys per tile (8 pages)
+constexpr int kTileRows = 128;     // rows per M tile
+constexpr int kCtaRows = 256;      // two M tiles per CTA
+constexpr int kPagesPerTile = kBlockN / 16;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: defer O rescale until max grows by 2^8
+constexpr float kLn2 = 0.69314718055994530942f;
+
+template <int D>
+struct Cfg {
+  static constexpr int kHalves = D / 64;                   // 128-byte column halves
+  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr uint32_t kHalfBytes = 128u * 128u;      // 128 rows x 128 B
+  static constexpr uint32_t kQTileBytes = kTileRows * D * 2;
+  static constexpr uint32_t kKVTileBytes = kBlockN * D * 2;
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffK = kOffQ + 2 * kQTileBytes;
+  static constexpr uint32_t kOffV = kOffK + kStages * kKVTileBytes;
+  static constexpr uint32_t kOffBar = kOffV + kStages * kKVTileBytes;
+  static constexpr uint32_t kBarBytes = 512;
+  static constexpr uint32_t kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128;
+  static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
+};
+
+struct Params {
+  const int* block_table;
+  const int* ctx_lens;
+  const int* cu_nodes;
+  const int* parents;
+  const int* kv_pages;
+  const int* cu_kv_pages;
+  __nv_bfloat16* out;
+  float* lse;
+  float* part_o;
+  float* part_lse;
+  int* err;
+  int num_q_heads;
+  int group;  // G
+  int num_pages;
+  int max_pages_per_seq;
+  int num_splits;
+  int total_nodes;
+  int groups_per_seq;
+  float scale_log2;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    tree_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
+                          const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_tk,
+                          const __grid_constant__ CUtensorMap tm_tv, const __grid_constant__ Params p) {
+  using C = Cfg<D>;
+  constexpr int NST = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int split = blockIdx.x;
+  const int kh = blockIdx.y / p.groups_per_seq;
+  const int mg = blockIdx.y % p.groups_per_seq;
+  const int b = blockIdx.z;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = p.group;
+
+  const int n0 = p.cu_nodes[b];
+  const int N = p.cu_nodes[b + 1] - n0;
+  const int L = p.ctx_lens[b];
+  const int rows_total = N * G;
+  const int row0 = mg * kCtaRows;
+  if (row0 >= rows_total) return;  // uniform: this row group does not exist
+  const bool tile1 = row0 + kTileRows < rows_total;
+  const bool partial = p.kv_pages != nullptr;
+  int n_pages, kvp0 = 0;
+  if (partial) {
+    kvp0 = p.cu_kv_pages[b];
+    n_pages = p.cu_kv_pages[b + 1] - kvp0;
+  } else {
+    n_pages = (L + 15) >> 4;
+  }
+  // Only the last listed page can hold fewer than 16 context tokens.
+  int last_page_tokens = 16;
+  if (n_pages > 0) {
+    const int lp = partial ? p.kv_pages[kvp0 + n_pages - 1] : n_pages - 1;
+    last_page_tokens = min(16, max(0, L - 16 * lp));
+  }
+  const int t_ctx = (n_pages + kPagesPerTile - 1) / kPagesPerTile;
+  const int t_all = t_ctx + 1;  // + the tree tile
+  const int jb = static_cast<int>(static_cast<long long>(split) * t_all / p.num_splits);
+  const int je = static_cast<int>(static_cast<long long>(split + 1) * t_all / p.num_splits);
+  const int ntiles = je - jb;
+
+  if (ntiles <= 0) {  // empty split: publish an empty partial for our rows
+    if (threadIdx.x < kCtaRows) {
+      const int row = row0 + threadIdx.x;
+      if (row < rows_total) {
+        const int node = row / G, g = row - (row / G) * G;
+        p.part_lse[(static_cast<size_t>(split) * p.total_nodes + n0 + node) * p.num_q_heads + kh * G + g] =
+            -INFINITY;
+      }
+    }
+    return;
+  }
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = k_full + NST;
+  uint64_t* k_empty = v_full + NST;
+  uint64_t* v_empty = k_empty + NST;
+  uint64_t* s_full = v_empty + NST;  // [2]
+  uint64_t* p_full = s_full + 2;     // [2]
+  uint64_t* o_final = p_full + 2;    // [2]
+  uint64_t* drain = o_final + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(k_full + i, 1);
+      mbar_init(v_full + i, 1);
+      mbar_init(k_empty + i, 1);
+      mbar_init(v_empty + i, 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(s_full + t, 1);
+      mbar_init(p_full + t, kTileRows);
+      mbar_init(o_final + t, 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kc);
+    tma_prefetch_desc(&tm_vc);
+    tma_prefetch_desc(&tm_tk);
+    tma_prefetch_desc(&tm_tv);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    regs_decrease<kRegsControl>();
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int issued = 0;
+    bool ok = true;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(q_full, (tile1 ? 2u : 1u) * C::kQTileBytes);
+      for (int t = 0; t < (tile1 ? 2 : 1); ++t)
+        for (int h = 0; h < C::kHalves; ++h)
+          tma_load_3d(smem + C::kOffQ + t * C::kQTileBytes + h * C::kHalfBytes, &tm_q, q_full, h * 64, kh * G,
+                      n0 + (row0 + t * kTileRows) / G);
+    }
+    for (int it = 0; it < ntiles; ++it) {
+      const int j = jb + it;
+      const int st = it % NST;
+      const uint32_t ph = (it / NST) & 1;
+      const bool ctx = j < t_ctx;
+      int phys = 0;
+      if (ctx && lane < kPagesPerTile) {
+        const int ps = min(j * kPagesPerTile + lane, n_pages - 1);  // ragged tail repeats the last page
+        int lp = partial ? p.kv_pages[kvp0 + ps] : ps;
+        if (lp < 0 || lp >= p.max_pages_per_seq) {
+          report_error(p.err, SV_DEVERR_BAD_PAGE);
+          lp = 0;
+        }
+        phys = p.block_table[static_cast<size_t>(b) * p.max_pages_per_seq + lp];
+        if (phys < 0 || phys >= p.num_pages) {
+          report_error(p.err, SV_DEVERR_BAD_PAGE);
+          phys = 0;
+        }
+      }
+      // K tile
+      if (it >= NST) {
+        int w = (lane == 0) ? (mbar_wait(k_empty + st, ph ^ 1u, abort_flag) ? 1 : 0) : 0;
+        if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+      }
+      if (lane == 0) mbar_arrive_expect_tx(k_full + st, C::kKVTileBytes);
+      __syncwarp();
+      uint8_t* kdst = smem + C::kOffK + st * C::kKVTileBytes;
+      if (ctx) {
+        if (lane < kPagesPerTile)
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_4d(kdst + h * C::kHalfBytes + lane * 2048, &tm_kc, k_full + st, h * 64, 0, kh, phys);
+      } else if (lane == 0) {
+        for (int h = 0; h < C::kHalves; ++h) tma_load_3d(kdst + h * C::kHalfBytes, &tm_tk, k_full + st, h * 64, kh, n0);
+      }
+      // V tile
+      if (it >= NST) {
+        int w = (lane == 0) ? (mbar_wait(v_empty + st, ph ^ 1u, abort_flag) ? 1 : 0) : 0;
+        if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; issued = it; break; }
+      }
+      if (lane == 0) mbar_arrive_expect_tx(v_full + st, C::kKVTileBytes);
+      __syncwarp();
+      uint8_t* vdst = smem + C::kOffV + st * C::kKVTileBytes;
+      if (ctx) {
+        if (lane < kPagesPerTile)
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_4d(vdst + h * C::kHalfBytes + lane * 2048, &tm_vc, v_full + st, h * 64, 0, kh, phys);
+      } else if (lane == 0) {
+        for (int h = 0; h < C::kHalves; ++h) tma_load_3d(vdst + h * C::kHalfBytes, &tm_tv, v_full + st, h * 64, kh, n0);
+      }
+      issued = it + 1;
+    }
+    if (!ok && lane == 0) {
+      // Timed out: stop the other roles, then let our copies land before exit.
+      report_error(p.err, SV_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+      for (int it = max(0, issued - NST); it < issued; ++it) {
+        mbar_wait(k_full + (it % NST), (it / NST) & 1, abort_flag);
+        mbar_wait(v_full + (it % NST), (it / NST) & 1, abort_flag);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kBlockN, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+      const int nt = tile1 ? 2 : 1;
+      const uint32_t q_base = smem_u32(smem + C::kOffQ);
+      const uint32_t k_base = smem_u32(smem + C::kOffK);
+      const uint32_t v_base = smem_u32(smem + C::kOffV);
+      bool ok = mbar_wait(q_full, 0, abort_flag);
+      auto issue_qk = [&](int t, int st) {
+        const uint32_t d = tmem + (t ? C::kColS1 : C::kColS0);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
+          const uint64_t a = smem_desc_sw128(q_base + t * C::kQTileBytes + off, 16, 1024);
+          const uint64_t bdesc = smem_desc_sw128(k_base + st * C::kKVTileBytes + off, 16, 1024);
+          umma_ss(d, a, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int t, int st, bool accumulate) {
+        const uint32_t d = tmem + (t ? C::kColO1 : C::kColO0);
+        const uint32_t a = tmem + (t ? C::kColS1 : C::kColS0);
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          const uint64_t bdesc = smem_desc_sw128(v_base + st * C::kKVTileBytes + kk * 2048, C::kHalfBytes, 1024);
+          umma_ts(d, a + kk * 8, bdesc, idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
+        }
+      };
+      if (ok) ok = mbar_wait(k_full, 0, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < nt; ++t) {
+          issue_qk(t, 0);
+          umma_commit(s_full + t);
+        }
+        umma_commit(k_empty);
+      }
+      for (int it = 0; ok && it < ntiles; ++it) {
+        const int st = it % NST;
+        const uint32_t ph = (it / NST) & 1;
+        const int nx = it + 1;
+        const int st2 = nx % NST;
+        const uint32_t ph2 = (nx / NST) & 1;
+        if (!mbar_wait(v_full + st, ph, abort_flag)) { ok = false; break; }
+        for (int t = 0; t < nt; ++t) {
+          if (!mbar_wait(p_full + t, it & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(t, st, it > 0);
+          if (nx < ntiles) {
+            if (t == 0) {
+              if (!mbar_wait(k_full + st2, ph2, abort_flag)) { ok = false; break; }
+              tc_fence_after();
+            }
+            issue_qk(t, st2);
+            umma_commit(s_full + t);
+          }
+        }
+        if (!ok) break;
+        umma_commit(v_empty + st);
+        if (nx < ntiles) umma_commit(k_empty + st2);
+      }
+      if (ok) {
+        for (int t = 0; t < nt; ++t) umma_commit(o_final + t);
+      } else {
+        report_error(p.err, SV_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+        umma_commit(drain);  // let issued MMAs finish before TMEM is freed
+        mbar_wait(drain, 0, abort_flag);
+      }
+    }
+    __syncwarp();
+  }
+  } else {
+    regs_increase<kRegsSoftmax>();
+    // ------------------------------------------------------------ softmax
+    const int t = (warp - 4) >> 2;
+    const int qw = warp & 3;
+    const int r = qw * 32 + lane;
+    if (t == 0 || tile1) {
+      const int row = row0 + t * kTileRows + r;
+      const bool row_valid = row < rows_total;
+      const int node = row / G;
+      const int g = row - node * G;
+      const uint32_t lane_base = tmem + (static_cast<uint32_t>(qw * 32) << 16);
+      const uint32_t col_s = t ? C::kColS1 : C::kColS0;
+      const uint32_t col_o = t ? C::kColO1 : C::kColO0;
+
+      // ancestor-or-self bitmask of this row's node (only the split that
+      // owns the tree tile needs it)
+      uint32_t anc0 = 0, anc1 = 0, anc2 = 0, anc3 = 0;
+      if (je == t_all && row_valid) {
+        int c = node;
+        for (int step = 0; step < kMaxNodes && c >= 0 && c < kMaxNodes; ++step) {
+          const uint32_t bit = 1u << (c & 31);
+          if ((c >> 5) == 0) anc0 |= bit;
+          else if ((c >> 5) == 1) anc1 |= bit;
+          else if ((c >> 5) == 2) anc2 |= bit;
+          else anc3 |= bit;
+          if (c == 0) break;
+          const int pc = p.parents[n0 + c];
+          if (pc < 0 || pc >= c) {
+            report_error(p.err, SV_DEVERR_BAD_PARENT);
+            break;
+          }
+          c = pc;
+        }
+      }
+
+      float m_run = -INFINITY;
+      float l_run = 0.f;
+      bool ok = true;
+      for (int it = 0; it < ntiles; ++it) {
+        const int j = jb + it;
+        if (!mbar_wait(s_full + t, it & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        float x[kBlockN];
+        {
+          uint32_t raw[32];
+#pragma unroll
+          for (int c = 0; c < kBlockN / 32; ++c) {
+            tmem_ld32(lane_base + col_s + c * 32, raw);
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) x[c * 32 + k] = __uint_as_float(raw[k]);
+          }
+        }
+        float tmax = -INFINITY;
+        if (j < t_ctx) {
+          const int nvalid =
+              (j == t_ctx - 1) ? ((n_pages - kPagesPerTile * j - 1) * 16 + last_page_tokens) : kBlockN;
+#pragma unroll
+          for (int k = 0; k < kBlockN; ++k) {
+            x[k] = (k < nvalid) ? x[k] * p.scale_log2 : -INFINITY;
+            tmax = fmaxf(tmax, x[k]);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < kBlockN; ++k) {
+            const uint32_t w = (k < 32) ? anc0 : (k < 64) ? anc1 : (k < 96) ? anc2 : anc3;
+            const bool vis = (k < N) && ((w >> (k & 31)) & 1u);
+            x[k] = vis ? x[k] * p.scale_log2 : -INFINITY;
+            tmax = fmaxf(tmax, x[k]);
+          }
+        }
+        const float m_new = fmaxf(m_run, tmax);
+        if (m_new > m_run + kRescaleThreshold) {
+          if (it > 0) {
+            // O already holds earlier tiles (their PV finished before this S
+            // was committed): rescale it and the running sum.
+            const float f = ex2(m_run - m_new);
+            l_run *= f;
+            uint32_t o[32];
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              tmem_ld32(lane_base + col_o + c * 32, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
+              tmem_st32(lane_base + col_o + c * 32, o);
+            }
+            tmem_st_wait();
+          }
+          m_run = m_new;
+        }
+        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        uint32_t pk[kBlockN / 2];
+        float lsum = 0.f;
+#pragma unroll
+        for (int k = 0; k < kBlockN; k += 2) {
+          const float p0 = ex2(x[k] - m_use);
+          const float p1 = ex2(x[k + 1] - m_use);
+          lsum += p0 + p1;
+          pk[k >> 1] = pack_bf16x2(p0, p1);
+        }
+        l_run += lsum;
+        {
+          uint32_t chunk[32];
+#pragma unroll
+          for (int c = 0; c < kBlockN / 64; ++c) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) chunk[k] = pk[c * 32 + k];
+            tmem_st32(lane_base + col_s + c * 32, chunk);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full + t);
+      }
+
+      // ---------------------------------------------------------- epilogue
+      if (ok) ok = mbar_wait(o_final + t, 0, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+        const size_t orow = static_cast<size_t>(n0 + node) * p.num_q_heads + kh * G + g;
+        if (p.num_splits == 1) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(lane_base + col_o + c * 32, o);
+            tmem_ld_wait();
+            if (row_valid) {
+              uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D + c * 32);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                uint4 w;
+                w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
+                w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
+                w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
+                w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
+                dst[v] = w;
+              }
+            }
+          }
+          if (row_valid && p.lse != nullptr) p.lse[orow] = (m_run + log2f(l_run)) * kLn2;
+        } else {
+          const size_t prow = static_cast<size_t>(split) * p.total_nodes * p.num_q_heads + orow;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(lane_base + col_o + c * 32, o);
+            tmem_ld_wait();
+            if (row_valid) {
+              float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D + c * 32);
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                     __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+            }
+          }
+          if (row_valid) p.part_lse[prow] = (l_run > 0.f) ? m_run + log2f(l_run) : -INFINITY;
+        }
+      } else if (lane == 0) {
+        report_error(p.err, SV_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// Merge split partials: O = sum_s w_s O_s / sum_s w_s, w_s = 2^(lse_s - max).
+template <int D>
+__global__ void __launch_bounds__(256) split_combine_kernel(const float* __restrict__ part_o,
+                                                            const float* __restrict__ part_lse,
+                                                            __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                                                            int rows, int splits) {
+  constexpr int E = D / 32;  // elements per lane
+  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float mx = -INFINITY;
+  for (int s = 0; s < splits; ++s) mx = fmaxf(mx, part_lse[static_cast<size_t>(s) * rows + row]);
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  for (int s = 0; s < splits; ++s) {
+    const float ls = part_lse[static_cast<size_t>(s) * rows + row];
+    if (ls == -INFINITY) continue;
+    const float w = ex2(ls - mx);
+    wsum += w;
+    const float* src = part_o + (static_cast<size_t>(s) * rows + row) * D + lane * E;
+    if constexpr (E == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      acc[0] += w * v.x;
+      acc[1] += w * v.y;
+      acc[2] += w * v.z;
+      acc[3] += w * v.w;
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(src);
+      acc[0] += w * v.x;
+      acc[1] += w * v.y;
+    }
+  }
+  const float inv = 1.f / wsum;
+  __nv_bfloat16* dst = out + static_cast<size_t>(row) * D + lane * E;
+  if constexpr (E == 4) {
+    uint2 w;
+    w.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    w.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(dst) = w;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  }
+  if (lse != nullptr && lane == 0) lse[row] = (mx + log2f(wsum)) * kLn2;
+}
+
+// ------------------------------------------------------------------ host
+
+struct Plan {
+  int group;
+  int groups_per_seq;
+  int splits;
+  size_t workspace;
+};
+
+sv_status validate(const sv_attn_params* p) {
+  if (p == nullptr) return SV_ERR_INVALID_ARG;
+  if (p->batch < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1 || p->total_nodes < 0 || p->max_nodes < 1 ||
+      p->max_pages_per_seq < 1 || p->num_pages < 1 || p->num_splits < 0 || p->max_kv_pages < 0)
+    return SV_ERR_INVALID_ARG;
+  if (p->num_q_heads % p->num_kv_heads != 0) return SV_ERR_INVALID_ARG;
+  const int G = p->num_q_heads / p->num_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return SV_ERR_UNSUPPORTED;
+  if (p->head_dim != 64 && p->head_dim != 128) return SV_ERR_UNSUPPORTED;
+  if (p->page_size != 16) return SV_ERR_UNSUPPORTED;
+  if (p->max_nodes > kMaxNodes) return SV_ERR_UNSUPPORTED;
+  if (p->num_splits > kMaxSplits) return SV_ERR_UNSUPPORTED;
+  if (!p->q || !p->tree_k || !p->tree_v || !p->k_cache || !p->v_cache || !p->block_table || !p->ctx_lens ||
+      !p->cu_nodes || !p->parents || !p->out)
+    return SV_ERR_INVALID_ARG;
+  if ((p->kv_pages == nullptr) != (p->cu_kv_pages == nullptr)) return SV_ERR_INVALID_ARG;
+  if (!aligned16(p->q) || !aligned16(p->tree_k) || !aligned16(p->tree_v) || !aligned16(p->k_cache) ||
+      !aligned16(p->v_cache) || !aligned16(p->out))
+    return SV_ERR_INVALID_ARG;
+  if (static_cast<long long>(p->batch) * p->num_kv_heads * ((p->max_nodes * G + kCtaRows - 1) / kCtaRows) > 65535)
+    return SV_ERR_UNSUPPORTED;
+  return SV_OK;
+}
+
+// Pick the number of KV splits: model the time as waves x per-CTA work, where
+// a CTA costs its share of KV tiles plus a fixed prologue/epilogue, and each
+// split adds a partial write + combine read.
+int choose_splits(const sv_attn_params* p, int sms, int groups_per_seq) {
+  if (p->num_splits > 0) return p->num_splits;
+  const long long units = static_cast<long long>(p->batch) * p->num_kv_heads * groups_per_seq;
+  const int pages = p->kv_pages ? p->max_kv_pages : p->max_pages_per_seq;
+  const int tiles = (pages + kPagesPerTile - 1) / kPagesPerTile + 1;
+  const double c_cta = 1.5, c_split = 0.75;
+  int best = 1;
+  double best_cost = 1e300;
+  for (int s = 1; s <= kMaxSplits && s <= tiles; ++s) {
+    const long long ctas = units * s;
+    const long long waves = (ctas + sms - 1) / sms;
+    double cost = static_cast<double>(waves) * (static_cast<double>(tiles) / s + c_cta);
+    if (s > 1) cost += c_split * static_cast<double>(ctas) / sms + 1.0;
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+sv_status make_plan(const sv_attn_params* p, Plan* plan) {
+  sv_status st = validate(p);
+  if (st != SV_OK) return st;
+  plan->group = p->num_q_heads / p->num_kv_heads;
+  plan->groups_per_seq = (p->max_nodes * plan->group + kCtaRows - 1) / kCtaRows;
+  int sms = 0;
+  if (p->num_splits == 0) {
+    sms = device_sm_count();
+    if (sms <= 0) return SV_ERR_CUDA;
+  }
+  plan->splits = choose_splits(p, sms, plan->groups_per_seq);
+  size_t ws = kWorkspaceHeader;
+  if (plan->splits > 1) {
+    const size_t rows = static_cast<size_t>(p->total_nodes) * p->num_q_heads;
+    ws += align_up(static_cast<size_t>(plan->splits) * rows * p->head_dim * sizeof(float), 256);
+    ws += align_up(static_cast<size_t>(plan->splits) * rows * sizeof(float), 256);
+  }
+  plan->workspace = ws;
+  return SV_OK;
+}
+
+template <int D>
+sv_status launch(const sv_attn_params* p, const Plan& plan, cudaStream_t stream) {
+  using C = Cfg<D>;
+  static std::mutex mu;
+  static bool configured[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 64 || !configured[dev]) {
+      if (cudaFuncSetAttribute(tree_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               C::kSmemBytes) != cudaSuccess)
+        return SV_ERR_CUDA;
+      if (dev < 64) configured[dev] = true;
+    }
+  }
+  const int G = plan.group;
+  const cuuint64_t T = static_cast<cuuint64_t>(p->total_nodes);
+  const cuuint64_t Hq = p->num_q_heads, Hkv = p->num_kv_heads, Dd = D, P = p->page_size;
+  CUtensorMap tm_q, tm_kc, tm_vc, tm_tk, tm_tv;
+  {
+    const cuuint64_t dims[3] = {Dd, Hq, T};
+    const cuuint64_t strides[2] = {Dd * 2, Hq * Dd * 2};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(kTileRows / G)};
+    if (encode_tiled(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p->q), dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B) != CUDA_SUCCESS)
+      return SV_ERR_CUDA;
+  }
+  {
+    const cuuint64_t dims[4] = {Dd, P, Hkv, static_cast<cuuint64_t>(p->num_pages)};
+    const cuuint64_t strides[3] = {Dd * 2, P * Dd * 2, Hkv * P * Dd * 2};
+    const cuuint32_t box[4] = {64, 16, 1, 1};
+    if (encode_tiled(&tm_kc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(p->k_cache), dims, strides,
+                     box, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != CUDA_SUCCESS)
+      return SV_ERR_CUDA;
+    if (encode_tiled(&tm_vc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(p->v_cache), dims, strides,
+                     box, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) != CUDA_SUCCESS)
+      return SV_ERR_CUDA;
+  }
+  {
+    const cuuint64_t dims[3] = {Dd, Hkv, T};
+    const cuuint64_t strides[2] = {Dd * 2, Hkv * Dd * 2};
+    const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kBlockN)};
+    if (encode_tiled(&tm_tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p->tree_k), dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B) != CUDA_SUCCESS)
+      return SV_ERR_CUDA;
+    if (encode_tiled(&tm_tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p->tree_v), dims, strides, box,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B) != CUDA_SUCCESS)
+      return SV_ERR_CUDA;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(p->workspace);
+  Params kp;
+  kp.block_table = p->block_table;
+  kp.ctx_lens = p->ctx_lens;
+  kp.cu_nodes = p->cu_nodes;
+  kp.parents = p->parents;
+  kp.kv_pages = p->kv_pages;
+  kp.cu_kv_pages = p->cu_kv_pages;
+  kp.out = static_cast<__nv_bfloat16*>(p->out);
+  kp.lse = p->lse;
+  kp.err = reinterpret_cast<int*>(ws);
+  const size_t rows = static_cast<size_t>(p->total_nodes) * p->num_q_heads;
+  kp.part_o = nullptr;
+  kp.part_lse = nullptr;
+  if (plan.splits > 1) {
+    kp.part_o = reinterpret_cast<float*>(ws + kWorkspaceHeader);
+    kp.part_lse = reinterpret_cast<float*>(
+        ws + kWorkspaceHeader + align_up(static_cast<size_t>(plan.splits) * rows * D * sizeof(float), 256));
+  }
+  kp.num_q_heads = p->num_q_heads;
+  kp.group = G;
+  kp.num_pages = p->num_pages;
+  kp.max_pages_per_seq = p->max_pages_per_seq;
+  kp.num_splits = plan.splits;
+  kp.total_nodes = p->total_nodes;
+  kp.groups_per_seq = plan.groups_per_seq;
+  const float scale = (p->sm_scale > 0.f) ? p->sm_scale : 1.0f / sqrtf(static_cast<float>(D));
+  kp.scale_log2 = scale * 1.4426950408889634f;
+
+  dim3 grid(plan.splits, p->num_kv_heads * plan.groups_per_seq, p->batch);
+  tree_attention_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tm_q, tm_kc, tm_vc, tm_tk, tm_tv, kp);
+  if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  if (plan.splits > 1) {
+    const int blocks = static_cast<int>((rows * 32 + 255) / 256);
+    split_combine_kernel<D><<<blocks, 256, 0, stream>>>(kp.part_o, kp.part_lse, kp.out, p->lse,
+                                                         static_cast<int>(rows), plan.splits);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  }
+  return SV_OK;
+}
+
+}  // namespace attn
+}  // namespace sv
+
+extern "C" {
+
+sv_status sv_tree_attention_workspace_size(const sv_attn_params* params, size_t* bytes) {
+  if (bytes == nullptr) return SV_ERR_INVALID_ARG;
+  sv::attn::Plan plan;
+  const sv_status st = sv::attn::make_plan(params, &plan);
+  if (st != SV_OK) return st;
+  *bytes = plan.workspace;
+  return SV_OK;
+}
+
+sv_status sv_tree_attention(const sv_attn_params* params, sv_stream_t stream) {
+  sv::attn::Plan plan;
+  const sv_status st = sv::attn::make_plan(params, &plan);
+  if (st != SV_OK) return st;
+  if (params->workspace == nullptr || params->workspace_bytes < plan.workspace) return SV_ERR_WORKSPACE;
+  if (params->total_nodes == 0) return SV_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (params->head_dim == 128) return sv::attn::launch<128>(params, plan, s);
+  return sv::attn::launch<64>(params, plan, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,120 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol
+``include/sv.h`` declares, and rejects bad host arguments synchronously
+(no CUDA call is made on these paths)."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from speculative_decoding_tree_sv_gb300 import binding, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "sv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:sv_status|int|const char\s*\*)\s+(sv_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_three_entry_points():
+    names = _declared()
+    for n in ("sv_tree_attention", "sv_greedy_accept", "sv_kv_commit"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", build.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    missing = [n for n in _declared() if n not in exported]
+    assert not missing, missing
+    for n in _declared():
+        assert hasattr(lib, n)
+
+
+def test_version_and_status_strings(lib):
+    assert binding.sv_abi_version() == 1
+    for code in range(7):
+        s = binding.sv_status_string(code)
+        assert s.startswith(binding.STATUS_NAMES[code])
+
+
+def _fake_params(**over):
+    # 16-byte aligned fake device addresses: host validation fails before use
+    a = 1 << 20
+    kw = dict(q=a, tree_k=a, tree_v=a, k_cache=a, v_cache=a, block_table=a, ctx_lens=a, cu_nodes=a,
+              parents=a, out=a, workspace=a, workspace_bytes=1 << 30, total_nodes=60, max_nodes=60,
+              batch=1, num_q_heads=32, num_kv_heads=8, head_dim=128, num_pages=300,
+              max_pages_per_seq=300, num_splits=4)
+    kw.update(over)
+    return binding.make_attn_params(**kw)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(head_dim=96), 2),
+    (dict(num_q_heads=24, num_kv_heads=8), 2),       # G = 3
+    (dict(num_q_heads=30, num_kv_heads=8), 1),       # not divisible
+    (dict(max_nodes=129), 2),
+    (dict(q=None), 1),
+    (dict(out=(1 << 20) + 8), 1),                    # misaligned
+    (dict(page_size=32), 2),
+    (dict(num_splits=65), 2),
+    (dict(workspace_bytes=16), 4),
+    (dict(kv_pages=1 << 20), 1),                     # list without prefix sums
+    (dict(batch=0), 1),
+])
+def test_attention_host_validation(lib, over, status):
+    p = _fake_params(**over)
+    assert lib.sv_tree_attention(ctypes.byref(p), None) == status
+
+
+def test_attention_workspace_size_with_explicit_splits(lib):
+    p = _fake_params(num_splits=4)
+    n = binding.sv_tree_attention_workspace_size(p)
+    rows = 60 * 32
+    assert n >= 256 + 4 * rows * 128 * 4 + 4 * rows * 4
+    p1 = _fake_params(num_splits=1)
+    assert binding.sv_tree_attention_workspace_size(p1) == 256
+
+
+def test_attention_null_params(lib):
+    assert lib.sv_tree_attention(None, None) == 1
+    n = ctypes.c_size_t(0)
+    assert lib.sv_tree_attention_workspace_size(None, ctypes.byref(n)) == 1
+
+
+def test_accept_host_validation(lib):
+    a = 1 << 20
+    need = binding.sv_greedy_accept_workspace_size(4, 100)
+    assert need >= 256 + 100 * 8 + 4 * 4
+    f = lib.sv_greedy_accept
+    assert f(None, 10, a, a, a, 1, 4, 4, 3, None, a, a, a, a, need, None) == 1
+    assert f(a, 10, a, a, a, 1, 4, 129, 3, None, a, a, a, a, need, None) == 2
+    assert f(a, 10, a, a, a, 4, 100, 4, 3, None, a, a, a, a, 16, None) == 4
+    assert f(a, 0, a, a, a, 1, 4, 4, 3, None, a, a, a, a, need, None) == 1
+
+
+def test_commit_host_validation(lib):
+    a = 1 << 20
+    f = lib.sv_kv_commit
+    base = [a, a, 1024, a, a, 4096, 2, 10, a, 4, a, a, a, a, 1, 3, 2, 64, 16]
+    # new_ctx_lens aliasing ctx_lens is rejected
+    args = base[:]
+    assert f(*args, a, None, 0, None) == 1
+    args = base[:]
+    args[2] = 1001  # stride not a multiple of 8
+    assert f(*args, None, None, 0, None) == 1
+    args = base[:]
+    args[17] = 60  # head_dim not a multiple of 8
+    assert f(*args, None, None, 0, None) == 2
+    args = base[:]
+    assert f(*args, None, a, 8, None) == 4  # workspace too small

@@ -1,0 +1,178 @@
+"""Bit-exact parity of sv_greedy_accept and sv_kv_commit (CUDA, through the
+C ABI) with the oracle: every workload's planted path, thousands of tiny
+random trees with duplicate sibling tokens and tied logits, ties across
+vocabulary chunks, signed zeros, repeated calls on one workspace, and the
+commit of every layer checked byte for byte with sentinel-filled caches."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import make_case
+from tests.gpu_support import DeviceCase, bf16, ensure_lib, i32, run_accept
+
+from speculative_decoding_tree_sv_gb300 import binding
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_lib()
+
+
+def _assert_accept_equal(res, ref, case):
+    assert res["err"] == 0
+    np.testing.assert_array_equal(res["argmax"], ref["argmax"])
+    np.testing.assert_array_equal(res["accept_len"], ref["accept_len"])
+    np.testing.assert_array_equal(res["bonus"], ref["bonus"])
+    for b in range(case.batch):
+        path = ref["accepted_nodes"][b]
+        row = res["accepted_nodes"][b]
+        assert list(row[: len(path)]) == path
+        assert (row[len(path):] == -1).all()
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("tiny", {}),
+    ("llama8b_eagle", dict(layers=1, ctx=16)),
+    ("serving_mix", dict(ctx=16)),
+    ("long_partial", dict(ctx=64, with_partial=False)),
+    ("specblock", dict(ctx=16)),
+])
+def test_workload_planted_paths(name, kw):
+    case = make_case(name, **kw)
+    ref = oracle.greedy_accept(case.logits, case.tokens, case.parents, case.cu_nodes)
+    res = run_accept(case)
+    _assert_accept_equal(res, ref, case)
+    np.testing.assert_array_equal(res["accept_len"], case.planted_len)
+    # the workspace was left ready: a second call gives the same answer
+    res2 = run_accept(case)
+    _assert_accept_equal(res2, ref, case)
+
+
+class _Tiny:
+    pass
+
+
+def _tiny_batch(rng, B, V, int_logits=True):
+    parents, tokens, rows, cu = [], [], [], [0]
+    for _ in range(B):
+        n = int(rng.integers(1, 10))
+        par = [-1] + [int(rng.integers(0, i)) for i in range(1, n)]
+        parents += par
+        tokens += rng.integers(0, V, size=n).tolist()
+        if int_logits:
+            lg = rng.integers(-1, 2, size=(n, V)).astype(np.float32)
+            z = lg == 0
+            lg[z] = np.where(rng.random(int(z.sum())) < 0.5, -0.0, 0.0)
+        else:
+            lg = rng.standard_normal((n, V)).astype(np.float32)
+        rows.append(lg)
+        cu.append(cu[-1] + n)
+    c = _Tiny()
+    c.logits = np.concatenate(rows)
+    c.tokens = np.array(tokens, np.int32)
+    c.parents = np.array(parents, np.int32)
+    c.cu_nodes = np.array(cu, np.int32)
+    c.batch, c.vocab = B, V
+    c.total_nodes = cu[-1]
+    c.max_nodes = int(np.diff(cu).max())
+    c.max_depth = 8
+    return c
+
+
+@pytest.mark.parametrize("V", [3, 4, 8, 13])
+def test_tiny_random_trees_with_ties_and_duplicates(V):
+    rng = np.random.default_rng(V)
+    for _ in range(40):
+        c = _tiny_batch(rng, 64, V)
+        ref = oracle.greedy_accept(c.logits, c.tokens, c.parents, c.cu_nodes)
+        _assert_accept_equal(run_accept(c), ref, c)
+
+
+def test_ties_across_vocabulary_chunks_and_signed_zero():
+    V = 20000
+    lg = np.full((4, V), -3.0, dtype=np.float32)
+    lg[0, [8191, 8192, 12345]] = 7.0        # lowest index wins across chunks
+    lg[1, [19999, 16384]] = 2.0
+    lg[2, :] = -0.0
+    lg[2, [5, 9000]] = 0.0                 # all zeros: index 0
+    lg[3, [3, 16383, 16384]] = 1.5
+    c = _Tiny()
+    c.logits, c.vocab, c.batch = lg, V, 4
+    c.tokens = np.zeros(4, np.int32)
+    c.parents = np.full(4, -1, np.int32)
+    c.cu_nodes = np.arange(5, dtype=np.int32)
+    c.total_nodes, c.max_nodes, c.max_depth = 4, 1, 0
+    res = run_accept(c)
+    assert list(res["argmax"]) == [8191, 16384, 0, 3]
+    ref = oracle.greedy_accept(lg, c.tokens, c.parents, c.cu_nodes)
+    _assert_accept_equal(res, ref, c)
+
+
+def test_full_size_logits_planted_paths():
+    for name in ("llama8b_eagle", "serving_mix", "specblock"):
+        case = make_case(name, layers=1, ctx=16)
+        ref = oracle.greedy_accept(case.logits, case.tokens, case.parents, case.cu_nodes)
+        _assert_accept_equal(run_accept(case), ref, case)
+
+
+def _commit_check(case, paths, alens, layers):
+    dc = DeviceCase(case, layers=layers)
+    L_ = len(layers)
+    T, Hkv, D = case.total_nodes, case.num_kv_heads, case.head_dim
+    md = case.max_depth
+    anodes = np.full((case.batch, md + 1), -1, np.int32)
+    for b, p in enumerate(paths):
+        anodes[b, : len(p)] = p
+    k_before = dc.k_cache.clone()
+    new_lens = torch.full((case.batch,), -1, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    binding.sv_kv_commit(dc.tree_k, dc.tree_v, T * Hkv * D, dc.k_cache, dc.v_cache,
+                         case.num_pages * Hkv * case.page_size * D, L_, case.num_pages, dc.block_table,
+                         case.max_pages_per_seq, dc.ctx_lens, dc.cu_nodes, i32(anodes), i32(alens),
+                         case.batch, md, Hkv, D, case.page_size, new_lens, ws)
+    torch.cuda.synchronize()
+    assert binding.sv_get_device_error(ws) == 0
+    k_ref, v_ref, lens_ref = oracle.kv_commit(case.k_cache[layers], case.v_cache[layers], case.tree_k[layers],
+                                              case.tree_v[layers], case.block_table, case.ctx_lens,
+                                              case.cu_nodes, paths, alens, case.page_size)
+    got_k = dc.k_cache.view(torch.int16).cpu().numpy().view(np.uint16)
+    got_v = dc.v_cache.view(torch.int16).cpu().numpy().view(np.uint16)
+    np.testing.assert_array_equal(got_k, k_ref)
+    np.testing.assert_array_equal(got_v, v_ref)
+    np.testing.assert_array_equal(new_lens.cpu().numpy(), lens_ref)
+    assert not torch.equal(k_before, dc.k_cache)
+
+
+def test_commit_all_layers_llama_eagle():
+    case = make_case("llama8b_eagle", layers=32, ctx=4096 - 3)  # slots cross a page boundary
+    ref = oracle.greedy_accept(case.logits, case.tokens, case.parents, case.cu_nodes)
+    _commit_check(case, ref["accepted_nodes"], ref["accept_len"], list(range(32)))
+
+
+def test_commit_serving_mix_ragged():
+    case = make_case("serving_mix", layers=1)
+    ref = oracle.greedy_accept(case.logits, case.tokens, case.parents, case.cu_nodes)
+    _commit_check(case, ref["accepted_nodes"], ref["accept_len"], [0])
+
+
+def test_commit_bad_path_is_reported():
+    case = make_case("tiny")
+    dc = DeviceCase(case)
+    T, Hkv, D = case.total_nodes, case.num_kv_heads, case.head_dim
+    anodes = np.full((1, case.max_depth + 1), -1, np.int32)
+    anodes[0, :3] = [0, 99, 1]  # node 99 does not exist
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    before = dc.k_cache.clone()
+    binding.sv_kv_commit(dc.tree_k, dc.tree_v, T * Hkv * D, dc.k_cache, dc.v_cache,
+                         case.num_pages * Hkv * 16 * D, 1, case.num_pages, dc.block_table,
+                         case.max_pages_per_seq, dc.ctx_lens, dc.cu_nodes, i32(anodes), i32([2]), 1,
+                         case.max_depth, Hkv, D, 16, None, ws)
+    torch.cuda.synchronize()
+    assert binding.sv_get_device_error(ws) == 4
+    # slots 0 and 2 of the path were written, slot 1 was skipped
+    changed = (before != dc.k_cache).any(dim=-1).any(dim=2).sum().item()
+    assert changed == 2

@@ -1,0 +1,162 @@
+"""Parity of sv_tree_attention (CUDA, through the C ABI) with the fp64
+oracle: |out - oracle| <= 2e-2 elementwise (bf16 inputs, fp32 accumulation),
+log-sum-exp within 2e-3.  Covers the five workloads (sampled where the
+oracle would take too long), several split counts, GQA groups 1..16, both
+head sizes, ragged and empty contexts, root-only and 128-node chain trees,
+partial page lists (empty, complete, SpecPV's small settings) and the
+device error word."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import make_case, tree_chain
+from tests.gpu_support import ATOL_ATTN, ATOL_LSE, DeviceCase, ensure_lib, run_attention
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_lib()
+
+
+def _oracle(case, li=0, partial=False, seqs=None, kv_heads=None, sm_scale=None):
+    return oracle.tree_verify_attention(
+        case.q[li], case.tree_k[li], case.tree_v[li], case.k_cache[li], case.v_cache[li], case.block_table,
+        case.ctx_lens, case.cu_nodes, case.parents, page_size=case.page_size,
+        kv_pages=case.kv_pages if partial else None, cu_kv_pages=case.cu_kv_pages if partial else None,
+        sm_scale=sm_scale, seqs=seqs, kv_heads=kv_heads)
+
+
+def _compare(case, out, lse, ref, ref_lse, seqs=None, kv_heads=None):
+    sel = ~np.isnan(ref_lse)
+    if seqs is None and kv_heads is None:
+        assert sel.all()
+    assert sel.any()
+    diff = np.abs(out - ref)[sel]
+    assert np.isfinite(out[sel]).all()
+    assert diff.max() <= ATOL_ATTN, f"max |diff| = {diff.max()}"
+    if lse is not None:
+        dl = np.abs(lse - ref_lse)[sel]
+        assert dl.max() <= ATOL_LSE, f"max |lse diff| = {dl.max()}"
+
+
+def _check(case, partial=False, num_splits=0, seqs=None, kv_heads=None, sm_scale=0.0, li=0):
+    dc = DeviceCase(case, layers=[li])
+    out, lse, _ = run_attention(dc, 0, partial=partial, num_splits=num_splits, sm_scale=sm_scale)
+    ref, ref_lse = _oracle(case, li, partial, seqs, kv_heads, sm_scale=sm_scale if sm_scale > 0 else None)
+    _compare(case, out, lse, ref, ref_lse, seqs, kv_heads)
+    return out
+
+
+@pytest.mark.parametrize("splits", [0, 1, 2, 5])
+def test_tiny(splits):
+    _check(make_case("tiny"), num_splits=splits)
+
+
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_llama_eagle_layer(splits):
+    _check(make_case("llama8b_eagle", layers=1, with_logits=False), num_splits=splits)
+
+
+def test_serving_mix_full_batch():
+    _check(make_case("serving_mix", with_logits=False))
+
+
+def test_long_context_partial_and_full():
+    case = make_case("long_partial", with_logits=False)
+    _check(case, partial=True)
+    _check(case, partial=False, kv_heads=[0, 5])
+
+
+def test_specblock_sampled():
+    case = make_case("specblock", with_logits=False)
+    _check(case, seqs=[0, 7, 15], kv_heads=[2, 6])
+
+
+def test_specblock_full_oracle_at_short_context():
+    _check(make_case("specblock", ctx=300, with_logits=False))
+
+
+@pytest.mark.parametrize("ctx", [[0], [1], [15], [17], [127], [129], [1000], [0, 33, 16, 200]])
+def test_ragged_and_empty_contexts(ctx):
+    case = make_case("tiny", batch=len(ctx), ctx=ctx, seed=sum(ctx) + 7, with_logits=False)
+    _check(case, num_splits=0)
+    _check(case, num_splits=3)
+
+
+def test_root_only_tree_is_decode_attention():
+    case = make_case("llama8b_eagle", layers=1, ctx=777, parents_list=[[-1]], with_logits=False)
+    _check(case)
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(8, 8, 128), (8, 4, 64), (16, 8, 128), (64, 8, 128), (32, 2, 64)])
+def test_group_sizes_and_head_dims(hq, hkv, d):
+    case = make_case("serving_mix", batch=3, ctx=(40, 300), num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
+                     with_logits=False, seed=hq * 100 + hkv)
+    _check(case)
+
+
+def test_chain_of_128_nodes():
+    case = make_case("tiny", num_q_heads=4, num_kv_heads=4, ctx=200, parents_list=[tree_chain(128)],
+                     with_logits=False)
+    _check(case)
+
+
+def test_128_nodes_at_group_8_spans_four_row_groups():
+    rng = np.random.default_rng(3)
+    par = [-1] + [int(rng.integers(0, i)) for i in range(1, 128)]
+    case = make_case("specblock", batch=2, ctx=[100, 40], parents_list=[par, par[:77]], with_logits=False)
+    _check(case)
+    _check(case, num_splits=4)
+
+
+@pytest.mark.parametrize("splits", [0, 2])
+def test_partial_lists_small_settings(splits):
+    # SpecPV Appendix D settings: 16-token blocks, 32 sink tokens, a 128-token
+    # window plus a 20-token buffer (folded into the recent window).
+    case = make_case("serving_mix", batch=4, ctx=(300, 900), with_logits=False,
+                     partial=dict(sink=32, blocks=6, block_tokens=16, recent=148))
+    _check(case, partial=True, num_splits=splits)
+
+
+def test_partial_all_pages_equals_full_and_empty_list():
+    case = make_case("tiny", batch=3, ctx=[203, 0, 64], with_logits=False)
+    lists = [np.arange(13), np.arange(0), np.arange(4)]
+    case.kv_pages = np.concatenate(lists).astype(np.int32)
+    case.cu_kv_pages = np.array([0, 13, 13, 17], np.int32)
+    part = _check(case, partial=True)
+    full = _check(case, partial=False)
+    np.testing.assert_array_equal(part, full)
+    # an empty list for every sequence: tree keys only
+    case.kv_pages = np.zeros(1, np.int32)
+    case.cu_kv_pages = np.zeros(4, np.int32)
+    _check(case, partial=True)
+
+
+def test_custom_scale():
+    _check(make_case("tiny", seed=9, with_logits=False), sm_scale=0.05)
+
+
+def test_bad_parent_is_reported_not_trapped():
+    case = make_case("tiny", with_logits=False)
+    case.parents = case.parents.copy()
+    case.parents[5] = 9  # parent after the child
+    dc = DeviceCase(case)
+    _, _, err = run_attention(dc, 0, check_error=False)
+    assert err == 2
+    # the context stays usable
+    good = make_case("tiny", with_logits=False)
+    _check(good)
+
+
+def test_bad_page_is_reported_not_trapped():
+    case = make_case("tiny", with_logits=False)
+    case.block_table = case.block_table.copy()
+    case.block_table[0, 3] = case.num_pages + 100  # beyond the pool
+    dc = DeviceCase(case)
+    _, _, err = run_attention(dc, 0, check_error=False)
+    assert err == 3
+    torch.cuda.synchronize()
