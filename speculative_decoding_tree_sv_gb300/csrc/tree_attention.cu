@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = o_final + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* never_set = abort_flag + 1;  // drains wait on copies even after an abort
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -171,6 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
+    *never_set = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_kc);
@@ -191,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_decrease<kRegsControl>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int issued = 0;
+    int k_issued = 0, v_issued = 0;
     bool ok = true;
     if (lane == 0) {
       mbar_arrive_expect_tx(q_full, (tile1 ? 2u : 1u) * C::kQTileBytes);
@@ -234,10 +236,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (lane == 0) {
         for (int h = 0; h < C::kHalves; ++h) tma_load_3d(kdst + h * C::kHalfBytes, &tm_tk, k_full + st, h * 64, kh, n0);
       }
+      k_issued = it + 1;
       // V tile
       if (it >= NST) {
         int w = (lane == 0) ? (mbar_wait(v_empty + st, ph ^ 1u, abort_flag) ? 1 : 0) : 0;
-        if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; issued = it; break; }
+        if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
       }
       if (lane == 0) mbar_arrive_expect_tx(v_full + st, C::kKVTileBytes);
       __syncwarp();
@@ -249,16 +252,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (lane == 0) {
         for (int h = 0; h < C::kHalves; ++h) tma_load_3d(vdst + h * C::kHalfBytes, &tm_tv, v_full + st, h * 64, kh, n0);
       }
-      issued = it + 1;
+      v_issued = it + 1;
     }
     if (!ok && lane == 0) {
       // Timed out: stop the other roles, then let our copies land before exit.
       report_error(p.err, SV_DEVERR_TIMEOUT);
       *abort_flag = 1;
-      for (int it = max(0, issued - NST); it < issued; ++it) {
-        mbar_wait(k_full + (it % NST), (it / NST) & 1, abort_flag);
-        mbar_wait(v_full + (it % NST), (it / NST) & 1, abort_flag);
-      }
+      mbar_wait(q_full, 0, never_set);
+      for (int it = max(0, k_issued - NST); it < k_issued; ++it)
+        mbar_wait(k_full + (it % NST), (it / NST) & 1, never_set);
+      for (int it = max(0, v_issued - NST); it < v_issued; ++it)
+        mbar_wait(v_full + (it % NST), (it / NST) & 1, never_set);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -328,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         report_error(p.err, SV_DEVERR_TIMEOUT);
         *abort_flag = 1;
         umma_commit(drain);  // let issued MMAs finish before TMEM is freed
-        mbar_wait(drain, 0, abort_flag);
+        mbar_wait(drain, 0, never_set);
       }
     }
     __syncwarp();
@@ -374,7 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int it = 0; it < ntiles; ++it) {
         const int j = jb + it;
-        if (!mbar_wait(s_full + t, it & 1, abort_flag)) { ok = false; break; }
+        // warp-uniform outcome: the TMEM loads below are warp-collective
+        if (!__all_sync(0xffffffffu, mbar_wait(s_full + t, it & 1, abort_flag))) { ok = false; break; }
         tc_fence_after();
         float x[kBlockN];
         {
@@ -451,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       // ---------------------------------------------------------- epilogue
-      if (ok) ok = mbar_wait(o_final + t, 0, abort_flag);
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_final + t, 0, abort_flag));
       if (ok) {
         tc_fence_after();
         const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
