@@ -432,8 +432,8 @@ def run_gpu(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["sv", "reference"], default="sv")
     ap.add_argument("--config", choices=sorted(WORKLOADS), default="llama8b_eagle")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -106,6 +106,11 @@ typedef struct sv_attn_params {
   int max_pages_per_seq;  /* row length of block_table                       */
   int max_kv_pages;       /* partial mode: max_b listed pages (host copy)    */
   int num_splits;         /* KV splits per (sequence, head group); 0 = auto  */
+  int split_reduce;       /* how splits merge: 0 = auto, 1 = on chip (the
+                             splits form a thread-block cluster and merge
+                             through distributed shared memory; num_splits
+                             <= 16), 2 = through workspace partials and a
+                             second kernel                                   */
   float sm_scale;         /* softmax scale; <= 0 selects 1/sqrt(D)           */
 
   /* tensors */

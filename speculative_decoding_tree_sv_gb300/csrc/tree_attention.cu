@@ -16,15 +16,22 @@
 //     ring of smem stages.  The tree's own K/V form one extra tile.
 //   * tcgen05.mma computes S = Q K^T (both operands K-major in smem) into
 //     TMEM; softmax warps read S with tcgen05.ld (one row per thread), apply
-//     the mask and an online, lazily rescaled softmax in base 2, write P as
-//     bf16 back into the S columns, and tcgen05.mma accumulates O += P V
-//     (P from TMEM, V MN-major in smem).
+//     the mask and an online, lazily rescaled softmax in base 2 (packed
+//     two-lane fp32 arithmetic), write P as bf16 back into the S columns, and
+//     tcgen05.mma accumulates O += P V (P from TMEM, V MN-major in smem).
 //   * Warp roles: warp 0 loads (TMA), warp 1 issues MMAs (one thread),
 //     warps 4-7 and 8-11 run the softmax of row tiles 0 and 1.  The MMA
 //     issue order S0 S1 | PV0 S0' | PV1 S1' ... keeps the tensor core busy
 //     while the two softmax groups alternate.
-//   * Splits of the KV range write (O / l, log2-sum-exp) partials that a
-//     second kernel merges; with one split the output is written directly.
+//   * KV splits are merged one of two ways.  On chip: the splits of one
+//     (sequence, head group) form a thread-block cluster; each CTA parks
+//     O / l and log2-sum-exp in its shared memory and every CTA merges a
+//     slice of the rows by reading its peers' shared memory (DSMEM), with
+//     mbarrier handshakes whose waits are bounded.  Through global memory:
+//     each split writes a partial that a second kernel merges (for very long
+//     contexts, where more splits than fit in co-resident clusters pay off).
+//   * Launches allow programmatic dependent launch: the prologue (barriers,
+//     TMEM, descriptor prefetch) runs before the wait on the previous grid.
 #include <math.h>
 
 #include <mutex>
@@ -43,8 +50,11 @@ constexpr int kBlockN = 128;       // keys per tile (8 pages)
 constexpr int kTileRows = 128;     // rows per M tile
 constexpr int kCtaRows = 256;      // two M tiles per CTA
 constexpr int kPagesPerTile = kBlockN / 16;
+constexpr int kMaxClusterSplits = 16;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: defer O rescale until max grows by 2^8
 constexpr float kLn2 = 0.69314718055994530942f;
+
+enum ReduceMode : int { kReduceNone = 0, kReduceCluster = 1, kReduceGlobal = 2 };
 
 template <int D>
 struct Cfg {
@@ -62,6 +72,12 @@ struct Cfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128;
   static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
+  // on-chip split merge: per-row O / l (fp32, padded rows) and log2-sum-exp,
+  // parked over the Q/K/V area once the main loop is done
+  static constexpr uint32_t kRedStride = D * 4 + 16;
+  static constexpr uint32_t kOffRedO = 0;
+  static constexpr uint32_t kOffRedL = kOffRedO + kCtaRows * kRedStride;
+  static_assert(kOffRedL + kCtaRows * 4 <= kOffBar, "merge buffer must fit below the barriers");
 };
 
 struct Params {
@@ -81,6 +97,7 @@ struct Params {
   int num_pages;
   int max_pages_per_seq;
   int num_splits;
+  int reduce_mode;
   int total_nodes;
   int groups_per_seq;
   float scale_log2;
@@ -103,13 +120,71 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.group;
+  const bool cluster_mode = p.reduce_mode == kReduceCluster;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = k_full + NST;
+  uint64_t* k_empty = v_full + NST;
+  uint64_t* v_empty = k_empty + NST;
+  uint64_t* s_full = v_empty + NST;  // [2]
+  uint64_t* p_full = s_full + 2;     // [2]
+  uint64_t* o_final = p_full + 2;    // [2]
+  uint64_t* drain = o_final + 2;
+  uint64_t* red_pub = drain + 1;     // cluster merge: peers published
+  uint64_t* red_done = red_pub + 1;  // cluster merge: peers finished reading
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* never_set = abort_flag + 1;  // drains wait on copies even after an abort
+
+  // ---- prologue that reads no input: it may overlap the previous grid
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(k_full + i, 1);
+      mbar_init(v_full + i, 1);
+      mbar_init(k_empty + i, 1);
+      mbar_init(v_empty + i, 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(s_full + t, 1);
+      mbar_init(p_full + t, kTileRows);
+      mbar_init(o_final + t, 1);
+    }
+    mbar_init(drain, 1);
+    mbar_init(red_pub, p.num_splits);
+    mbar_init(red_done, p.num_splits);
+    *abort_flag = 0;
+    *never_set = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_kc);
+    tma_prefetch_desc(&tm_vc);
+    tma_prefetch_desc(&tm_tk);
+    tma_prefetch_desc(&tm_tv);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  // every CTA of a cluster reaches this point: peers' barriers are initialised
+  // before anyone can arrive on them remotely
+  if (cluster_mode) cluster_sync_all();
+  const uint32_t tmem = *tmem_slot;
+  griddep_wait();
+  griddep_launch_dependents();
 
   const int n0 = p.cu_nodes[b];
   const int N = p.cu_nodes[b + 1] - n0;
   const int L = p.ctx_lens[b];
   const int rows_total = N * G;
   const int row0 = mg * kCtaRows;
-  if (row0 >= rows_total) return;  // uniform: this row group does not exist
+  // uniform over the cluster (its CTAs differ only in the split)
+  if (row0 < rows_total) {
   const bool tile1 = row0 + kTileRows < rows_total;
   const bool partial = p.kv_pages != nullptr;
   int n_pages, kvp0 = 0;
@@ -130,8 +205,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int jb = static_cast<int>(static_cast<long long>(split) * t_all / p.num_splits);
   const int je = static_cast<int>(static_cast<long long>(split + 1) * t_all / p.num_splits);
   const int ntiles = je - jb;
+  const bool work = ntiles > 0;
 
-  if (ntiles <= 0) {  // empty split: publish an empty partial for our rows
+  if (!work && p.reduce_mode == kReduceGlobal) {
+    // empty split: publish an empty partial for our rows
     if (threadIdx.x < kCtaRows) {
       const int row = row0 + threadIdx.x;
       if (row < rows_total) {
@@ -140,370 +217,421 @@ __global__ void __launch_bounds__(kThreads, 1)
             -INFINITY;
       }
     }
-    return;
-  }
-
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;
-  uint64_t* v_full = k_full + NST;
-  uint64_t* k_empty = v_full + NST;
-  uint64_t* v_empty = k_empty + NST;
-  uint64_t* s_full = v_empty + NST;  // [2]
-  uint64_t* p_full = s_full + 2;     // [2]
-  uint64_t* o_final = p_full + 2;    // [2]
-  uint64_t* drain = o_final + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* never_set = abort_flag + 1;  // drains wait on copies even after an abort
-
-  if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int i = 0; i < NST; ++i) {
-      mbar_init(k_full + i, 1);
-      mbar_init(v_full + i, 1);
-      mbar_init(k_empty + i, 1);
-      mbar_init(v_empty + i, 1);
-    }
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(s_full + t, 1);
-      mbar_init(p_full + t, kTileRows);
-      mbar_init(o_final + t, 1);
-    }
-    mbar_init(drain, 1);
-    *abort_flag = 0;
-    *never_set = 0;
-    fence_mbar_init();
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_kc);
-    tma_prefetch_desc(&tm_vc);
-    tma_prefetch_desc(&tm_tk);
-    tma_prefetch_desc(&tm_tv);
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, C::kTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp < 4) {
+  } else if (warp < 4) {
     regs_decrease<kRegsControl>();
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    int k_issued = 0, v_issued = 0;
-    bool ok = true;
-    if (lane == 0) {
-      mbar_arrive_expect_tx(q_full, (tile1 ? 2u : 1u) * C::kQTileBytes);
-      for (int t = 0; t < (tile1 ? 2 : 1); ++t)
-        for (int h = 0; h < C::kHalves; ++h)
-          tma_load_3d(smem + C::kOffQ + t * C::kQTileBytes + h * C::kHalfBytes, &tm_q, q_full, h * 64, kh * G,
-                      n0 + (row0 + t * kTileRows) / G);
-    }
-    for (int it = 0; it < ntiles; ++it) {
-      const int j = jb + it;
-      const int st = it % NST;
-      const uint32_t ph = (it / NST) & 1;
-      const bool ctx = j < t_ctx;
-      int phys = 0;
-      if (ctx && lane < kPagesPerTile) {
-        const int ps = min(j * kPagesPerTile + lane, n_pages - 1);  // ragged tail repeats the last page
-        int lp = partial ? p.kv_pages[kvp0 + ps] : ps;
-        if (lp < 0 || lp >= p.max_pages_per_seq) {
-          report_error(p.err, SV_DEVERR_BAD_PAGE);
-          lp = 0;
-        }
-        phys = p.block_table[static_cast<size_t>(b) * p.max_pages_per_seq + lp];
-        if (phys < 0 || phys >= p.num_pages) {
-          report_error(p.err, SV_DEVERR_BAD_PAGE);
-          phys = 0;
-        }
-      }
-      // K tile
-      if (it >= NST) {
-        int w = (lane == 0) ? (mbar_wait(k_empty + st, ph ^ 1u, abort_flag) ? 1 : 0) : 0;
-        if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
-      }
-      if (lane == 0) mbar_arrive_expect_tx(k_full + st, C::kKVTileBytes);
-      __syncwarp();
-      uint8_t* kdst = smem + C::kOffK + st * C::kKVTileBytes;
-      if (ctx) {
-        if (lane < kPagesPerTile)
+    if (work && warp == 0) {
+      // ------------------------------------------------------------ producer
+      int k_issued = 0, v_issued = 0;
+      bool ok = true;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(q_full, (tile1 ? 2u : 1u) * C::kQTileBytes);
+        for (int t = 0; t < (tile1 ? 2 : 1); ++t)
           for (int h = 0; h < C::kHalves; ++h)
-            tma_load_4d(kdst + h * C::kHalfBytes + lane * 2048, &tm_kc, k_full + st, h * 64, 0, kh, phys);
-      } else if (lane == 0) {
-        for (int h = 0; h < C::kHalves; ++h) tma_load_3d(kdst + h * C::kHalfBytes, &tm_tk, k_full + st, h * 64, kh, n0);
+            tma_load_3d(smem + C::kOffQ + t * C::kQTileBytes + h * C::kHalfBytes, &tm_q, q_full, h * 64, kh * G,
+                        n0 + (row0 + t * kTileRows) / G);
       }
-      k_issued = it + 1;
-      // V tile
-      if (it >= NST) {
-        int w = (lane == 0) ? (mbar_wait(v_empty + st, ph ^ 1u, abort_flag) ? 1 : 0) : 0;
-        if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
-      }
-      if (lane == 0) mbar_arrive_expect_tx(v_full + st, C::kKVTileBytes);
-      __syncwarp();
-      uint8_t* vdst = smem + C::kOffV + st * C::kKVTileBytes;
-      if (ctx) {
-        if (lane < kPagesPerTile)
-          for (int h = 0; h < C::kHalves; ++h)
-            tma_load_4d(vdst + h * C::kHalfBytes + lane * 2048, &tm_vc, v_full + st, h * 64, 0, kh, phys);
-      } else if (lane == 0) {
-        for (int h = 0; h < C::kHalves; ++h) tma_load_3d(vdst + h * C::kHalfBytes, &tm_tv, v_full + st, h * 64, kh, n0);
-      }
-      v_issued = it + 1;
-    }
-    if (!ok && lane == 0) {
-      // Timed out: stop the other roles, then let our copies land before exit.
-      report_error(p.err, SV_DEVERR_TIMEOUT);
-      *abort_flag = 1;
-      mbar_wait(q_full, 0, never_set);
-      for (int it = max(0, k_issued - NST); it < k_issued; ++it)
-        mbar_wait(k_full + (it % NST), (it / NST) & 1, never_set);
-      for (int it = max(0, v_issued - NST); it < v_issued; ++it)
-        mbar_wait(v_full + (it % NST), (it / NST) & 1, never_set);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kBlockN, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
-      const int nt = tile1 ? 2 : 1;
-      const uint32_t q_base = smem_u32(smem + C::kOffQ);
-      const uint32_t k_base = smem_u32(smem + C::kOffK);
-      const uint32_t v_base = smem_u32(smem + C::kOffV);
-      bool ok = mbar_wait(q_full, 0, abort_flag);
-      auto issue_qk = [&](int t, int st) {
-        const uint32_t d = tmem + (t ? C::kColS1 : C::kColS0);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-          const uint64_t a = smem_desc_sw128(q_base + t * C::kQTileBytes + off, 16, 1024);
-          const uint64_t bdesc = smem_desc_sw128(k_base + st * C::kKVTileBytes + off, 16, 1024);
-          umma_ss(d, a, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
-        }
-      };
-      auto issue_pv = [&](int t, int st, bool accumulate) {
-        const uint32_t d = tmem + (t ? C::kColO1 : C::kColO0);
-        const uint32_t a = tmem + (t ? C::kColS1 : C::kColS0);
-#pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          const uint64_t bdesc = smem_desc_sw128(v_base + st * C::kKVTileBytes + kk * 2048, C::kHalfBytes, 1024);
-          umma_ts(d, a + kk * 8, bdesc, idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
-        }
-      };
-      if (ok) ok = mbar_wait(k_full, 0, abort_flag);
-      if (ok) {
-        tc_fence_after();
-        for (int t = 0; t < nt; ++t) {
-          issue_qk(t, 0);
-          umma_commit(s_full + t);
-        }
-        umma_commit(k_empty);
-      }
-      for (int it = 0; ok && it < ntiles; ++it) {
+      for (int it = 0; it < ntiles; ++it) {
+        const int j = jb + it;
         const int st = it % NST;
         const uint32_t ph = (it / NST) & 1;
-        const int nx = it + 1;
-        const int st2 = nx % NST;
-        const uint32_t ph2 = (nx / NST) & 1;
-        if (!mbar_wait(v_full + st, ph, abort_flag)) { ok = false; break; }
-        for (int t = 0; t < nt; ++t) {
-          if (!mbar_wait(p_full + t, it & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          issue_pv(t, st, it > 0);
-          if (nx < ntiles) {
-            if (t == 0) {
-              if (!mbar_wait(k_full + st2, ph2, abort_flag)) { ok = false; break; }
-              tc_fence_after();
-            }
-            issue_qk(t, st2);
-            umma_commit(s_full + t);
+        const bool ctx = j < t_ctx;
+        int phys = 0;
+        if (ctx && lane < kPagesPerTile) {
+          const int ps = min(j * kPagesPerTile + lane, n_pages - 1);  // ragged tail repeats the last page
+          int lp = partial ? p.kv_pages[kvp0 + ps] : ps;
+          if (lp < 0 || lp >= p.max_pages_per_seq) {
+            report_error(p.err, SV_DEVERR_BAD_PAGE);
+            lp = 0;
+          }
+          phys = p.block_table[static_cast<size_t>(b) * p.max_pages_per_seq + lp];
+          if (phys < 0 || phys >= p.num_pages) {
+            report_error(p.err, SV_DEVERR_BAD_PAGE);
+            phys = 0;
           }
         }
-        if (!ok) break;
-        umma_commit(v_empty + st);
-        if (nx < ntiles) umma_commit(k_empty + st2);
+        // K tile
+        if (it >= NST) {
+          int w = (lane == 0) ? (mbar_wait(k_empty + st, ph ^ 1u, abort_flag) ? 1 : 0) : 0;
+          if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+        }
+        if (lane == 0) mbar_arrive_expect_tx(k_full + st, C::kKVTileBytes);
+        __syncwarp();
+        uint8_t* kdst = smem + C::kOffK + st * C::kKVTileBytes;
+        if (ctx) {
+          if (lane < kPagesPerTile)
+            for (int h = 0; h < C::kHalves; ++h)
+              tma_load_4d(kdst + h * C::kHalfBytes + lane * 2048, &tm_kc, k_full + st, h * 64, 0, kh, phys);
+        } else if (lane == 0) {
+          for (int h = 0; h < C::kHalves; ++h) tma_load_3d(kdst + h * C::kHalfBytes, &tm_tk, k_full + st, h * 64, kh, n0);
+        }
+        k_issued = it + 1;
+        // V tile
+        if (it >= NST) {
+          int w = (lane == 0) ? (mbar_wait(v_empty + st, ph ^ 1u, abort_flag) ? 1 : 0) : 0;
+          if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+        }
+        if (lane == 0) mbar_arrive_expect_tx(v_full + st, C::kKVTileBytes);
+        __syncwarp();
+        uint8_t* vdst = smem + C::kOffV + st * C::kKVTileBytes;
+        if (ctx) {
+          if (lane < kPagesPerTile)
+            for (int h = 0; h < C::kHalves; ++h)
+              tma_load_4d(vdst + h * C::kHalfBytes + lane * 2048, &tm_vc, v_full + st, h * 64, 0, kh, phys);
+        } else if (lane == 0) {
+          for (int h = 0; h < C::kHalves; ++h) tma_load_3d(vdst + h * C::kHalfBytes, &tm_tv, v_full + st, h * 64, kh, n0);
+        }
+        v_issued = it + 1;
       }
-      if (ok) {
-        for (int t = 0; t < nt; ++t) umma_commit(o_final + t);
-      } else {
+      if (!ok && lane == 0) {
+        // Timed out: stop the other roles, then let our copies land before exit.
         report_error(p.err, SV_DEVERR_TIMEOUT);
         *abort_flag = 1;
-        umma_commit(drain);  // let issued MMAs finish before TMEM is freed
-        mbar_wait(drain, 0, never_set);
+        mbar_wait(q_full, 0, never_set);
+        for (int it = max(0, k_issued - NST); it < k_issued; ++it)
+          mbar_wait(k_full + (it % NST), (it / NST) & 1, never_set);
+        for (int it = max(0, v_issued - NST); it < v_issued; ++it)
+          mbar_wait(v_full + (it % NST), (it / NST) & 1, never_set);
       }
+    } else if (work && warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kBlockN, false, false);
+        constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+        const int nt = tile1 ? 2 : 1;
+        const uint32_t q_base = smem_u32(smem + C::kOffQ);
+        const uint32_t k_base = smem_u32(smem + C::kOffK);
+        const uint32_t v_base = smem_u32(smem + C::kOffV);
+        bool ok = mbar_wait(q_full, 0, abort_flag);
+        auto issue_qk = [&](int t, int st) {
+          const uint32_t d = tmem + (t ? C::kColS1 : C::kColS0);
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
+            const uint64_t a = smem_desc_sw128(q_base + t * C::kQTileBytes + off, 16, 1024);
+            const uint64_t bdesc = smem_desc_sw128(k_base + st * C::kKVTileBytes + off, 16, 1024);
+            umma_ss(d, a, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+          }
+        };
+        auto issue_pv = [&](int t, int st, bool accumulate) {
+          const uint32_t d = tmem + (t ? C::kColO1 : C::kColO0);
+          const uint32_t a = tmem + (t ? C::kColS1 : C::kColS0);
+  #pragma unroll
+          for (int kk = 0; kk < kBlockN / 16; ++kk) {
+            const uint64_t bdesc = smem_desc_sw128(v_base + st * C::kKVTileBytes + kk * 2048, C::kHalfBytes, 1024);
+            umma_ts(d, a + kk * 8, bdesc, idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
+          }
+        };
+        if (ok) ok = mbar_wait(k_full, 0, abort_flag);
+        if (ok) {
+          tc_fence_after();
+          for (int t = 0; t < nt; ++t) {
+            issue_qk(t, 0);
+            umma_commit(s_full + t);
+          }
+          umma_commit(k_empty);
+        }
+        for (int it = 0; ok && it < ntiles; ++it) {
+          const int st = it % NST;
+          const uint32_t ph = (it / NST) & 1;
+          const int nx = it + 1;
+          const int st2 = nx % NST;
+          const uint32_t ph2 = (nx / NST) & 1;
+          if (!mbar_wait(v_full + st, ph, abort_flag)) { ok = false; break; }
+          for (int t = 0; t < nt; ++t) {
+            if (!mbar_wait(p_full + t, it & 1, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(t, st, it > 0);
+            if (nx < ntiles) {
+              if (t == 0) {
+                if (!mbar_wait(k_full + st2, ph2, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+              }
+              issue_qk(t, st2);
+              umma_commit(s_full + t);
+            }
+          }
+          if (!ok) break;
+          umma_commit(v_empty + st);
+          if (nx < ntiles) umma_commit(k_empty + st2);
+        }
+        if (ok) {
+          for (int t = 0; t < nt; ++t) umma_commit(o_final + t);
+        } else {
+          report_error(p.err, SV_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+          umma_commit(drain);  // let issued MMAs finish before TMEM is freed
+          mbar_wait(drain, 0, never_set);
+        }
+      }
+      __syncwarp();
     }
-    __syncwarp();
-  }
   } else {
     regs_increase<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
     const int t = (warp - 4) >> 2;
     const int qw = warp & 3;
     const int r = qw * 32 + lane;
-    if (t == 0 || tile1) {
-      const int row = row0 + t * kTileRows + r;
-      const bool row_valid = row < rows_total;
-      const int node = row / G;
-      const int g = row - node * G;
-      const uint32_t lane_base = tmem + (static_cast<uint32_t>(qw * 32) << 16);
-      const uint32_t col_s = t ? C::kColS1 : C::kColS0;
-      const uint32_t col_o = t ? C::kColO1 : C::kColO0;
-
-      // ancestor-or-self bitmask of this row's node (only the split that
-      // owns the tree tile needs it)
-      uint32_t anc0 = 0, anc1 = 0, anc2 = 0, anc3 = 0;
-      if (je == t_all && row_valid) {
-        int c = node;
-        for (int step = 0; step < kMaxNodes && c >= 0 && c < kMaxNodes; ++step) {
-          const uint32_t bit = 1u << (c & 31);
-          if ((c >> 5) == 0) anc0 |= bit;
-          else if ((c >> 5) == 1) anc1 |= bit;
-          else if ((c >> 5) == 2) anc2 |= bit;
-          else anc3 |= bit;
-          if (c == 0) break;
-          const int pc = p.parents[n0 + c];
-          if (pc < 0 || pc >= c) {
-            report_error(p.err, SV_DEVERR_BAD_PARENT);
-            break;
-          }
-          c = pc;
-        }
-      }
-
-      float m_run = -INFINITY;
-      float l_run = 0.f;
-      bool ok = true;
-      for (int it = 0; it < ntiles; ++it) {
-        const int j = jb + it;
-        // warp-uniform outcome: the TMEM loads below are warp-collective
-        if (!__all_sync(0xffffffffu, mbar_wait(s_full + t, it & 1, abort_flag))) { ok = false; break; }
-        tc_fence_after();
-        float x[kBlockN];
-        {
-          uint32_t raw[32];
-#pragma unroll
-          for (int c = 0; c < kBlockN / 32; ++c) {
-            tmem_ld32(lane_base + col_s + c * 32, raw);
-            tmem_ld_wait();
-#pragma unroll
-            for (int k = 0; k < 32; ++k) x[c * 32 + k] = __uint_as_float(raw[k]);
-          }
-        }
-        float tmax = -INFINITY;
-        if (j < t_ctx) {
-          const int nvalid =
-              (j == t_ctx - 1) ? ((n_pages - kPagesPerTile * j - 1) * 16 + last_page_tokens) : kBlockN;
-#pragma unroll
-          for (int k = 0; k < kBlockN; ++k) {
-            x[k] = (k < nvalid) ? x[k] * p.scale_log2 : -INFINITY;
-            tmax = fmaxf(tmax, x[k]);
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < kBlockN; ++k) {
-            const uint32_t w = (k < 32) ? anc0 : (k < 64) ? anc1 : (k < 96) ? anc2 : anc3;
-            const bool vis = (k < N) && ((w >> (k & 31)) & 1u);
-            x[k] = vis ? x[k] * p.scale_log2 : -INFINITY;
-            tmax = fmaxf(tmax, x[k]);
-          }
-        }
-        const float m_new = fmaxf(m_run, tmax);
-        if (m_new > m_run + kRescaleThreshold) {
-          if (it > 0) {
-            // O already holds earlier tiles (their PV finished before this S
-            // was committed): rescale it and the running sum.
-            const float f = ex2(m_run - m_new);
-            l_run *= f;
-            uint32_t o[32];
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              tmem_ld32(lane_base + col_o + c * 32, o);
-              tmem_ld_wait();
-#pragma unroll
-              for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
-              tmem_st32(lane_base + col_o + c * 32, o);
+    const int r_cta = t * kTileRows + r;
+    const int row = row0 + r_cta;
+    const bool row_exists = row < rows_total;
+    const bool active = work && (t == 0 || tile1);  // warp-uniform
+    const int node = row / G;
+    const int g = row - node * G;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(qw * 32) << 16);
+    const uint32_t col_s = t ? C::kColS1 : C::kColS0;
+    const uint32_t col_o = t ? C::kColO1 : C::kColO0;
+    float m_run = -INFINITY;
+    float l_run = 0.f;
+    bool ok = true;
+    if (active) {
+        // ancestor-or-self bitmask of this row's node (only the split that
+        // owns the tree tile needs it)
+        uint32_t anc0 = 0, anc1 = 0, anc2 = 0, anc3 = 0;
+        if (je == t_all && row_exists) {
+          int c = node;
+          for (int step = 0; step < kMaxNodes && c >= 0 && c < kMaxNodes; ++step) {
+            const uint32_t bit = 1u << (c & 31);
+            if ((c >> 5) == 0) anc0 |= bit;
+            else if ((c >> 5) == 1) anc1 |= bit;
+            else if ((c >> 5) == 2) anc2 |= bit;
+            else anc3 |= bit;
+            if (c == 0) break;
+            const int pc = p.parents[n0 + c];
+            if (pc < 0 || pc >= c) {
+              report_error(p.err, SV_DEVERR_BAD_PARENT);
+              break;
             }
-            tmem_st_wait();
-          }
-          m_run = m_new;
-        }
-        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        uint32_t pk[kBlockN / 2];
-        float lsum = 0.f;
-#pragma unroll
-        for (int k = 0; k < kBlockN; k += 2) {
-          const float p0 = ex2(x[k] - m_use);
-          const float p1 = ex2(x[k + 1] - m_use);
-          lsum += p0 + p1;
-          pk[k >> 1] = pack_bf16x2(p0, p1);
-        }
-        l_run += lsum;
-        {
-          uint32_t chunk[32];
-#pragma unroll
-          for (int c = 0; c < kBlockN / 64; ++c) {
-#pragma unroll
-            for (int k = 0; k < 32; ++k) chunk[k] = pk[c * 32 + k];
-            tmem_st32(lane_base + col_s + c * 32, chunk);
+            c = pc;
           }
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(p_full + t);
-      }
 
-      // ---------------------------------------------------------- epilogue
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_final + t, 0, abort_flag));
-      if (ok) {
-        tc_fence_after();
-        const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
-        const size_t orow = static_cast<size_t>(n0 + node) * p.num_q_heads + kh * G + g;
-        if (p.num_splits == 1) {
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(lane_base + col_o + c * 32, o);
-            tmem_ld_wait();
-            if (row_valid) {
-              uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D + c * 32);
-#pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                uint4 w;
-                w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
-                w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
-                w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
-                w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
-                dst[v] = w;
+        for (int it = 0; it < ntiles; ++it) {
+          const int j = jb + it;
+          // warp-uniform outcome: the TMEM loads below are warp-collective
+          if (!__all_sync(0xffffffffu, mbar_wait(s_full + t, it & 1, abort_flag))) { ok = false; break; }
+          tc_fence_after();
+          uint32_t sr[kBlockN];
+  #pragma unroll
+          for (int c = 0; c < kBlockN / 32; ++c)
+            tmem_ld32(lane_base + col_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
+          tmem_ld_wait();
+          // mask: only the ragged last context tile and the tree tile need one
+          constexpr uint32_t kNegInf = 0xFF800000u;
+          if (j >= t_ctx) {
+  #pragma unroll
+            for (int k = 0; k < kBlockN; ++k) {
+              const uint32_t w = (k < 32) ? anc0 : (k < 64) ? anc1 : (k < 96) ? anc2 : anc3;
+              if (!((k < N) && ((w >> (k & 31)) & 1u))) sr[k] = kNegInf;
+            }
+          } else if (j == t_ctx - 1) {
+            const int nvalid = (n_pages - kPagesPerTile * j - 1) * 16 + last_page_tokens;
+  #pragma unroll
+            for (int k = 0; k < kBlockN; ++k)
+              if (k >= nvalid) sr[k] = kNegInf;
+          }
+          // row maximum of the raw scores (scale > 0 commutes with max)
+          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+  #pragma unroll
+          for (int k = 0; k < kBlockN; k += 8) {
+            mx0 = max3(mx0, __uint_as_float(sr[k + 0]), __uint_as_float(sr[k + 1]));
+            mx1 = max3(mx1, __uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3]));
+            mx2 = max3(mx2, __uint_as_float(sr[k + 4]), __uint_as_float(sr[k + 5]));
+            mx3 = max3(mx3, __uint_as_float(sr[k + 6]), __uint_as_float(sr[k + 7]));
+          }
+          const float tmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
+          const float m_new = fmaxf(m_run, tmax);
+          if (m_new > m_run + kRescaleThreshold) {
+            if (it > 0) {
+              // O already holds earlier tiles (their PV finished before this S
+              // was committed): rescale it and the running sum.
+              const float f = ex2(m_run - m_new);
+              l_run *= f;
+              const uint64_t f2 = f2_pack(f, f);
+              uint32_t o[32];
+  #pragma unroll
+              for (int c = 0; c < D / 32; ++c) {
+                tmem_ld32(lane_base + col_o + c * 32, o);
+                tmem_ld_wait();
+  #pragma unroll
+                for (int k = 0; k < 32; k += 2) {
+                  const uint64_t v = f2_mul(f2_pack(__uint_as_float(o[k]), __uint_as_float(o[k + 1])), f2);
+                  o[k] = static_cast<uint32_t>(v);
+                  o[k + 1] = static_cast<uint32_t>(v >> 32);
+                }
+                tmem_st32(lane_base + col_o + c * 32, o);
               }
+              tmem_st_wait();
             }
+            m_run = m_new;
           }
-          if (row_valid && p.lse != nullptr) p.lse[orow] = (m_run + log2f(l_run)) * kLn2;
-        } else {
-          const size_t prow = static_cast<size_t>(split) * p.total_nodes * p.num_q_heads + orow;
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(lane_base + col_o + c * 32, o);
-            tmem_ld_wait();
-            if (row_valid) {
-              float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D + c * 32);
-#pragma unroll
-              for (int v = 0; v < 8; ++v)
-                dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
-                                     __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
-            }
+          const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+          // p = 2^(s * scale_log2 - m), packed two at a time
+          const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+          const uint64_t nm2 = f2_pack(-m_use, -m_use);
+          uint64_t acc0 = 0, acc1 = 0;
+          uint32_t pk[kBlockN / 2];
+  #pragma unroll
+          for (int k = 0; k < kBlockN; k += 4) {
+            const uint64_t a = f2_fma(f2_pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), sc2, nm2);
+            const uint64_t b = f2_fma(f2_pack(__uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3])), sc2, nm2);
+            const float p0 = ex2(f2_lo(a)), p1 = ex2(f2_hi(a));
+            const float p2 = ex2(f2_lo(b)), p3 = ex2(f2_hi(b));
+            acc0 = f2_add(acc0, f2_pack(p0, p1));
+            acc1 = f2_add(acc1, f2_pack(p2, p3));
+            pk[k >> 1] = pack_bf16x2(p0, p1);
+            pk[(k >> 1) + 1] = pack_bf16x2(p2, p3);
           }
-          if (row_valid) p.part_lse[prow] = (l_run > 0.f) ? m_run + log2f(l_run) : -INFINITY;
+          const uint64_t acc = f2_add(acc0, acc1);
+          l_run += f2_lo(acc) + f2_hi(acc);
+  #pragma unroll
+          for (int c = 0; c < kBlockN / 64; ++c)
+            tmem_st32(lane_base + col_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(pk + c * 32));
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(p_full + t);
         }
-      } else if (lane == 0) {
+
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_final + t, 0, abort_flag));
+      if (!ok && lane == 0) {
         report_error(p.err, SV_DEVERR_TIMEOUT);
         *abort_flag = 1;
       }
     }
+
+    // ---------------------------------------------------------- epilogue
+    const bool have_o = active && ok;  // warp-uniform
+    if (have_o) tc_fence_after();
+    const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
+    const float lse2 = (have_o && l_run > 0.f) ? m_run + log2f(l_run) : -INFINITY;
+    const size_t orow = static_cast<size_t>(n0 + node) * p.num_q_heads + kh * G + g;
+    if (p.reduce_mode == kReduceNone) {
+      if (have_o) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + col_o + c * 32, o);
+          tmem_ld_wait();
+          if (row_exists) {
+            uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D + c * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
+              w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
+              w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
+              w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
+              dst[v] = w;
+            }
+          }
+        }
+        if (row_exists && p.lse != nullptr) p.lse[orow] = lse2 * kLn2;
+      }
+    } else if (p.reduce_mode == kReduceGlobal) {
+      if (have_o) {
+        const size_t prow = static_cast<size_t>(split) * p.total_nodes * p.num_q_heads + orow;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + col_o + c * 32, o);
+          tmem_ld_wait();
+          if (row_exists) {
+            float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D + c * 32);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                   __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+          }
+        }
+        if (row_exists) p.part_lse[prow] = lse2;
+      } else if (row_exists && (t == 0 || tile1)) {
+        p.part_lse[static_cast<size_t>(split) * p.total_nodes * p.num_q_heads + orow] = -INFINITY;
+      }
+    } else {
+      // ---- on-chip merge across the cluster (one CTA per split)
+      float* red_o = reinterpret_cast<float*>(smem + C::kOffRedO);
+      float* red_l = reinterpret_cast<float*>(smem + C::kOffRedL);
+      if (have_o) {
+        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(red_o) + r_cta * C::kRedStride);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + col_o + c * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[c * 8 + v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                         __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+        }
+      }
+      red_l[r_cta] = lse2;
+      fence_acq_rel_cluster();
+      named_barrier(1, 2 * kTileRows);
+      const int S = p.num_splits;
+      if (threadIdx.x == 4 * 32) {
+        for (int rk = 0; rk < S; ++rk) mbar_arrive_cluster(mapa_shared(smem_u32(red_pub), rk));
+      }
+      if (mbar_wait_cluster(red_pub, 0)) {
+        constexpr int E = D / 32;  // output elements per lane
+        const int rank = static_cast<int>(cluster_ctarank());
+        const int rows_cta = min(kCtaRows, rows_total - row0);
+        const int slice = (rows_cta + S - 1) / S;
+        const int lo = rank * slice, hi = min(rows_cta, lo + slice);
+        const uint32_t o_base = smem_u32(red_o), l_base = smem_u32(red_l);
+        for (int rr = lo + (warp - 4); rr < hi; rr += 8) {
+          const float ls = (lane < S) ? ld_dsmem_f32(mapa_shared(l_base + rr * 4, lane)) : -INFINITY;
+          float mx = ls;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          const float w = (ls == -INFINITY) ? 0.f : ex2(ls - mx);
+          float wsum = w;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+          float acc[E];
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[e] = 0.f;
+          for (int s = 0; s < S; ++s) {
+            const float ws = __shfl_sync(0xffffffffu, w, s);
+            if (ws == 0.f) continue;
+            const uint32_t a = mapa_shared(o_base + rr * C::kRedStride + lane * E * 4, s);
+            if constexpr (E == 4) {
+              const float4 v = ld_dsmem_f32x4(a);
+              acc[0] += ws * v.x;
+              acc[1] += ws * v.y;
+              acc[2] += ws * v.z;
+              acc[3] += ws * v.w;
+            } else {
+              const float2 v = ld_dsmem_f32x2(a);
+              acc[0] += ws * v.x;
+              acc[1] += ws * v.y;
+            }
+          }
+          const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
+          const int grow = row0 + rr;
+          const int gnode = grow / G;
+          const size_t out_row = static_cast<size_t>(n0 + gnode) * p.num_q_heads + kh * G + (grow - gnode * G);
+          __nv_bfloat16* dst = p.out + out_row * D + lane * E;
+          if constexpr (E == 4) {
+            uint2 v;
+            v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+            v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+            *reinterpret_cast<uint2*>(dst) = v;
+          } else {
+            *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+          }
+          if (lane == 0 && p.lse != nullptr) p.lse[out_row] = (mx + log2f(wsum)) * kLn2;
+        }
+      } else if (lane == 0) {
+        report_error(p.err, SV_DEVERR_TIMEOUT);
+      }
+      // peers may read our shared memory until every CTA has finished reading
+      named_barrier(1, 2 * kTileRows);
+      if (threadIdx.x == 4 * 32) {
+        for (int rk = 0; rk < S; ++rk) mbar_arrive_cluster(mapa_shared(smem_u32(red_done), rk));
+      }
+      if (!mbar_wait_cluster(red_done, 0) && lane == 0) report_error(p.err, SV_DEVERR_TIMEOUT);
+    }
   }
+  }  // row group exists
 
   tc_fence_before();
   __syncthreads();
@@ -566,13 +694,15 @@ struct Plan {
   int group;
   int groups_per_seq;
   int splits;
+  int mode;
   size_t workspace;
 };
 
 sv_status validate(const sv_attn_params* p) {
   if (p == nullptr) return SV_ERR_INVALID_ARG;
   if (p->batch < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1 || p->total_nodes < 0 || p->max_nodes < 1 ||
-      p->max_pages_per_seq < 1 || p->num_pages < 1 || p->num_splits < 0 || p->max_kv_pages < 0)
+      p->max_pages_per_seq < 1 || p->num_pages < 1 || p->num_splits < 0 || p->max_kv_pages < 0 ||
+      p->split_reduce < 0 || p->split_reduce > 2)
     return SV_ERR_INVALID_ARG;
   if (p->num_q_heads % p->num_kv_heads != 0) return SV_ERR_INVALID_ARG;
   const int G = p->num_q_heads / p->num_kv_heads;
@@ -581,6 +711,7 @@ sv_status validate(const sv_attn_params* p) {
   if (p->page_size != 16) return SV_ERR_UNSUPPORTED;
   if (p->max_nodes > kMaxNodes) return SV_ERR_UNSUPPORTED;
   if (p->num_splits > kMaxSplits) return SV_ERR_UNSUPPORTED;
+  if (p->split_reduce == 1 && p->num_splits > kMaxClusterSplits) return SV_ERR_UNSUPPORTED;
   if (!p->q || !p->tree_k || !p->tree_v || !p->k_cache || !p->v_cache || !p->block_table || !p->ctx_lens ||
       !p->cu_nodes || !p->parents || !p->out)
     return SV_ERR_INVALID_ARG;
@@ -593,28 +724,130 @@ sv_status validate(const sv_attn_params* p) {
   return SV_OK;
 }
 
-// Pick the number of KV splits: model the time as waves x per-CTA work, where
-// a CTA costs its share of KV tiles plus a fixed prologue/epilogue, and each
-// split adds a partial write + combine read.
-int choose_splits(const sv_attn_params* p, int sms, int groups_per_seq) {
-  if (p->num_splits > 0) return p->num_splits;
+template <int D>
+void launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attrs, dim3 grid, int cluster, cudaStream_t s) {
+  *cfg = cudaLaunchConfig_t{};
+  cfg->gridDim = grid;
+  cfg->blockDim = dim3(kThreads, 1, 1);
+  cfg->dynamicSmemBytes = Cfg<D>::kSmemBytes;
+  cfg->stream = s;
+  int n = 0;
+  attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster > 1) {
+    attrs[n].id = cudaLaunchAttributeClusterDimension;
+    attrs[n].val.clusterDim.x = cluster;
+    attrs[n].val.clusterDim.y = 1;
+    attrs[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg->attrs = attrs;
+  cfg->numAttrs = n;
+}
+
+// One-time per-device kernel attributes (dynamic smem, cluster size > 8).
+template <int D>
+bool configure_kernel() {
+  static std::mutex mu;
+  static bool done[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 64 && done[dev]) return true;
+  if (cudaFuncSetAttribute(tree_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<D>::kSmemBytes) != cudaSuccess)
+    return false;
+  if (cudaFuncSetAttribute(tree_attention_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+      cudaSuccess)
+    return false;
+  if (dev < 64) done[dev] = true;
+  return true;
+}
+
+// Co-resident clusters of `size` CTAs at this kernel's footprint (cached per
+// device); 0 when they cannot be scheduled or the query fails.
+template <int D>
+int max_active_clusters(int size) {
+  static std::mutex mu;
+  static int cache[64][kMaxClusterSplits + 1];
+  static bool init = false;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!init) {
+    for (auto& row : cache)
+      for (int& v : row) v = -1;
+    init = true;
+  }
+  if (cache[dev][size] >= 0) return cache[dev][size];
+  int n = 0;
+  if (configure_kernel<D>()) {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attrs[2];
+    launch_config<D>(&cfg, attrs, dim3(size, 1, 1), size, nullptr);
+    if (cudaOccupancyMaxActiveClusters(&n, tree_attention_kernel<D>, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();
+  cache[dev][size] = n;
+  return n;
+}
+
+int active_clusters(int head_dim, int size) {
+  return head_dim == 128 ? max_active_clusters<128>(size) : max_active_clusters<64>(size);
+}
+
+// Split count and merge mode from a small cost model in units of one KV tile
+// of work: a CTA costs its share of tiles plus a fixed prologue/epilogue;
+// waves come from how many CTAs (or clusters) are co-resident; an on-chip
+// merge costs a little per CTA, a global merge costs partial writes plus a
+// second kernel.
+void choose_splits(const sv_attn_params* p, int sms, int groups_per_seq, int* splits, int* mode) {
   const long long units = static_cast<long long>(p->batch) * p->num_kv_heads * groups_per_seq;
   const int pages = p->kv_pages ? p->max_kv_pages : p->max_pages_per_seq;
   const int tiles = (pages + kPagesPerTile - 1) / kPagesPerTile + 1;
-  const double c_cta = 1.5, c_split = 0.75;
-  int best = 1;
-  double best_cost = 1e300;
-  for (int s = 1; s <= kMaxSplits && s <= tiles; ++s) {
-    const long long ctas = units * s;
-    const long long waves = (ctas + sms - 1) / sms;
-    double cost = static_cast<double>(waves) * (static_cast<double>(tiles) / s + c_cta);
-    if (s > 1) cost += c_split * static_cast<double>(ctas) / sms + 1.0;
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
-      best = s;
+  const double c_cta = 1.5, c_red = 0.75, c_part = 1.0, c_comb = 2.0;
+  auto cost_cluster = [&](int s) -> double {
+    const int act = active_clusters(p->head_dim, s);
+    if (act <= 0) return 1e300;
+    const long long waves = (units + act - 1) / act;
+    return static_cast<double>(waves) * (static_cast<double>(tiles) / s + c_cta + c_red);
+  };
+  auto cost_global = [&](int s) -> double {
+    const long long waves = (units * s + sms - 1) / sms;
+    return static_cast<double>(waves) * (static_cast<double>(tiles) / s + c_cta + c_part) + c_comb + 0.05 * s;
+  };
+  if (p->num_splits > 0) {
+    *splits = p->num_splits;
+    if (*splits == 1) *mode = kReduceNone;
+    else if (p->split_reduce == 2) *mode = kReduceGlobal;
+    else if (p->split_reduce == 1) *mode = kReduceCluster;
+    else *mode = (*splits <= 8 || (*splits <= kMaxClusterSplits && sms > 0 && active_clusters(p->head_dim, *splits) > 0))
+                     ? kReduceCluster : kReduceGlobal;
+    return;
+  }
+  const long long waves1 = (units + sms - 1) / sms;
+  double best = static_cast<double>(waves1) * (tiles + c_cta);
+  *splits = 1;
+  *mode = kReduceNone;
+  for (int s = 2; s <= kMaxSplits && s <= tiles; ++s) {
+    if (p->split_reduce != 2 && s <= kMaxClusterSplits) {
+      const double c = cost_cluster(s);
+      if (c < best - 1e-9) {
+        best = c;
+        *splits = s;
+        *mode = kReduceCluster;
+      }
+    }
+    if (p->split_reduce != 1) {
+      const double c = cost_global(s);
+      if (c < best - 1e-9) {
+        best = c;
+        *splits = s;
+        *mode = kReduceGlobal;
+      }
     }
   }
-  return best;
 }
 
 sv_status make_plan(const sv_attn_params* p, Plan* plan) {
@@ -623,13 +856,13 @@ sv_status make_plan(const sv_attn_params* p, Plan* plan) {
   plan->group = p->num_q_heads / p->num_kv_heads;
   plan->groups_per_seq = (p->max_nodes * plan->group + kCtaRows - 1) / kCtaRows;
   int sms = 0;
-  if (p->num_splits == 0) {
+  if (p->num_splits == 0 || (p->num_splits > 8 && p->split_reduce == 0)) {
     sms = device_sm_count();
     if (sms <= 0) return SV_ERR_CUDA;
   }
-  plan->splits = choose_splits(p, sms, plan->groups_per_seq);
+  choose_splits(p, sms, plan->groups_per_seq, &plan->splits, &plan->mode);
   size_t ws = kWorkspaceHeader;
-  if (plan->splits > 1) {
+  if (plan->mode == kReduceGlobal) {
     const size_t rows = static_cast<size_t>(p->total_nodes) * p->num_q_heads;
     ws += align_up(static_cast<size_t>(plan->splits) * rows * p->head_dim * sizeof(float), 256);
     ws += align_up(static_cast<size_t>(plan->splits) * rows * sizeof(float), 256);
@@ -640,20 +873,7 @@ sv_status make_plan(const sv_attn_params* p, Plan* plan) {
 
 template <int D>
 sv_status launch(const sv_attn_params* p, const Plan& plan, cudaStream_t stream) {
-  using C = Cfg<D>;
-  static std::mutex mu;
-  static bool configured[64] = {false};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev >= 64 || !configured[dev]) {
-      if (cudaFuncSetAttribute(tree_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               C::kSmemBytes) != cudaSuccess)
-        return SV_ERR_CUDA;
-      if (dev < 64) configured[dev] = true;
-    }
-  }
+  if (!configure_kernel<D>()) return SV_ERR_CUDA;
   const int G = plan.group;
   const cuuint64_t T = static_cast<cuuint64_t>(p->total_nodes);
   const cuuint64_t Hq = p->num_q_heads, Hkv = p->num_kv_heads, Dd = D, P = p->page_size;
@@ -702,7 +922,7 @@ sv_status launch(const sv_attn_params* p, const Plan& plan, cudaStream_t stream)
   const size_t rows = static_cast<size_t>(p->total_nodes) * p->num_q_heads;
   kp.part_o = nullptr;
   kp.part_lse = nullptr;
-  if (plan.splits > 1) {
+  if (plan.mode == kReduceGlobal) {
     kp.part_o = reinterpret_cast<float*>(ws + kWorkspaceHeader);
     kp.part_lse = reinterpret_cast<float*>(
         ws + kWorkspaceHeader + align_up(static_cast<size_t>(plan.splits) * rows * D * sizeof(float), 256));
@@ -712,15 +932,19 @@ sv_status launch(const sv_attn_params* p, const Plan& plan, cudaStream_t stream)
   kp.num_pages = p->num_pages;
   kp.max_pages_per_seq = p->max_pages_per_seq;
   kp.num_splits = plan.splits;
+  kp.reduce_mode = plan.mode;
   kp.total_nodes = p->total_nodes;
   kp.groups_per_seq = plan.groups_per_seq;
   const float scale = (p->sm_scale > 0.f) ? p->sm_scale : 1.0f / sqrtf(static_cast<float>(D));
   kp.scale_log2 = scale * 1.4426950408889634f;
 
-  dim3 grid(plan.splits, p->num_kv_heads * plan.groups_per_seq, p->batch);
-  tree_attention_kernel<D><<<grid, kThreads, C::kSmemBytes, stream>>>(tm_q, tm_kc, tm_vc, tm_tk, tm_tv, kp);
-  if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
-  if (plan.splits > 1) {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attrs[2];
+  launch_config<D>(&cfg, attrs, dim3(plan.splits, p->num_kv_heads * plan.groups_per_seq, p->batch),
+                   plan.mode == kReduceCluster ? plan.splits : 1, stream);
+  if (cudaLaunchKernelEx(&cfg, tree_attention_kernel<D>, tm_q, tm_kc, tm_vc, tm_tk, tm_tv, kp) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (plan.mode == kReduceGlobal) {
     const int blocks = static_cast<int>((rows * 32 + 255) / 256);
     split_combine_kernel<D><<<blocks, 256, 0, stream>>>(kp.part_o, kp.part_lse, kp.out, p->lse,
                                                          static_cast<int>(rows), plan.splits);

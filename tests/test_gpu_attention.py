@@ -43,22 +43,27 @@ def _compare(case, out, lse, ref, ref_lse, seqs=None, kv_heads=None):
         assert dl.max() <= ATOL_LSE, f"max |lse diff| = {dl.max()}"
 
 
-def _check(case, partial=False, num_splits=0, seqs=None, kv_heads=None, sm_scale=0.0, li=0):
+def _check(case, partial=False, num_splits=0, seqs=None, kv_heads=None, sm_scale=0.0, li=0, split_reduce=0):
     dc = DeviceCase(case, layers=[li])
-    out, lse, _ = run_attention(dc, 0, partial=partial, num_splits=num_splits, sm_scale=sm_scale)
+    out, lse, _ = run_attention(dc, 0, partial=partial, num_splits=num_splits, sm_scale=sm_scale,
+                                split_reduce=split_reduce)
     ref, ref_lse = _oracle(case, li, partial, seqs, kv_heads, sm_scale=sm_scale if sm_scale > 0 else None)
     _compare(case, out, lse, ref, ref_lse, seqs, kv_heads)
     return out
 
 
-@pytest.mark.parametrize("splits", [0, 1, 2, 5])
-def test_tiny(splits):
-    _check(make_case("tiny"), num_splits=splits)
+@pytest.mark.parametrize("splits,mode", [(0, 0), (1, 0), (2, 1), (5, 1), (5, 2), (7, 1)])
+def test_tiny(splits, mode):
+    # more splits than tiles leaves some splits empty
+    _check(make_case("tiny"), num_splits=splits, split_reduce=mode)
 
 
-@pytest.mark.parametrize("splits", [0, 1, 3])
-def test_llama_eagle_layer(splits):
-    _check(make_case("llama8b_eagle", layers=1, with_logits=False), num_splits=splits)
+@pytest.mark.parametrize("splits,mode", [(0, 0), (1, 0), (3, 1), (3, 2), (10, 1), (16, 1), (19, 2), (34, 2),
+                                         (2, 1), (9, 1)])
+def test_llama_eagle_layer(splits, mode):
+    # mode 1: splits merged on chip through the cluster's shared memory;
+    # mode 2: through workspace partials and a combine kernel
+    _check(make_case("llama8b_eagle", layers=1, with_logits=False), num_splits=splits, split_reduce=mode)
 
 
 def test_serving_mix_full_batch():
@@ -68,7 +73,9 @@ def test_serving_mix_full_batch():
 def test_long_context_partial_and_full():
     case = make_case("long_partial", with_logits=False)
     _check(case, partial=True)
+    _check(case, partial=True, num_splits=12, split_reduce=1)
     _check(case, partial=False, kv_heads=[0, 5])
+    _check(case, partial=False, kv_heads=[3], num_splits=16, split_reduce=1)
 
 
 def test_specblock_sampled():
@@ -85,6 +92,7 @@ def test_ragged_and_empty_contexts(ctx):
     case = make_case("tiny", batch=len(ctx), ctx=ctx, seed=sum(ctx) + 7, with_logits=False)
     _check(case, num_splits=0)
     _check(case, num_splits=3)
+    _check(case, num_splits=3, split_reduce=2)
 
 
 def test_root_only_tree_is_decode_attention():
@@ -111,6 +119,7 @@ def test_128_nodes_at_group_8_spans_four_row_groups():
     case = make_case("specblock", batch=2, ctx=[100, 40], parents_list=[par, par[:77]], with_logits=False)
     _check(case)
     _check(case, num_splits=4)
+    _check(case, num_splits=4, split_reduce=2)
 
 
 @pytest.mark.parametrize("splits", [0, 2])
