@@ -203,7 +203,7 @@ class GpuStep:
         self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
         for p in self.params:
             p.workspace, p.workspace_bytes = self.ws.data_ptr(), ws_bytes
-        self.splits = self._splits(ws_bytes)
+        self.splits, self.split_reduce = binding.sv_tree_attention_plan(self.params[0])
         B = c.batch
         self.am = torch.empty(self.T, dtype=torch.int32, device=dev)
         self.alen = torch.empty(B, dtype=torch.int32, device=dev)
@@ -213,13 +213,8 @@ class GpuStep:
                                   device=dev)
         self.new_lens = torch.empty(B, dtype=torch.int32, device=dev)
 
-    def _splits(self, ws_bytes):
-        rows = self.T * self.Hq
-        per_split = rows * self.D * 4 + rows * 4
-        return max(1, round((ws_bytes - 256) / per_split)) if ws_bytes > 256 else 1
-
     def launches_per_step(self):
-        per_attn = 2 if self.splits > 1 else 1
+        per_attn = 2 if self.split_reduce == 2 else 1
         return self.layers * per_attn + 2
 
     def attention_all_layers(self):
@@ -409,7 +404,9 @@ def run_gpu(args):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOADS[args.config], "layers": c.num_layers, "batch": c.batch,
-                       "total_nodes": c.total_nodes, "kv_splits": st.splits, "cuda_graph": True,
+                       "total_nodes": c.total_nodes, "kv_splits": st.splits,
+                       "split_merge": ["none", "on-chip cluster", "global partials"][st.split_reduce],
+                       "cuda_graph": True,
                        "l2": "inputs larger than L2 (distinct KV per layer, %.0f MB per step)"
                              % (sum(ctx_keys) * 4 * c.num_kv_heads * c.head_dim * c.num_layers / 1e6),
                        "parallelism": "replicas" if world > 1 else "single GPU"},

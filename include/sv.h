@@ -139,6 +139,11 @@ typedef struct sv_attn_params {
  * the current device's SM count when num_splits == 0). */
 sv_status sv_tree_attention_workspace_size(const sv_attn_params* params, size_t* bytes);
 
+/* The launch plan sv_tree_attention would use for these parameters: the
+ * number of KV splits and how they merge (0 = single split, 1 = on chip
+ * through the cluster's shared memory, 2 = through workspace partials). */
+sv_status sv_tree_attention_plan(const sv_attn_params* params, int* num_splits, int* split_reduce);
+
 /* Launches the attention (and, with more than one split, the split combine)
  * on `stream`.  Grid: one CTA per (KV split, KV head x 256-row group,
  * sequence); see the library's design notes for the kernel. */
@@ -206,6 +211,34 @@ sv_status sv_kv_commit(const void* tree_k, const void* tree_v, long long tree_la
                        int max_depth, int num_kv_heads, int head_dim, int page_size,
                        int* new_ctx_lens, void* workspace, size_t workspace_bytes,
                        sv_stream_t stream);
+
+/* Diagnostics: per-CTA phase tracing of sv_tree_attention.
+ *
+ * After this call, every sv_tree_attention launch (until the buffer is
+ * replaced, or removed with buffer = NULL) writes, for each of its CTAs in
+ * linear grid order, kSvTraceSlots 64-bit words: [0] %globaltimer (ns) at
+ * CTA start, [1..] SM clock cycles since CTA start at the phase boundaries
+ * listed in sv_trace_event.  A CTA beyond the buffer records nothing.  The
+ * setting is process-wide and not synchronised with launches in flight; use
+ * it from one thread while no launch is being recorded into a stream. */
+enum { kSvTraceSlots = 16 };
+typedef enum sv_trace_event {
+  SV_TRACE_START_NS = 0,      /* globaltimer at CTA start                      */
+  SV_TRACE_PROLOGUE = 1,      /* barriers, TMEM and descriptor prefetch done   */
+  SV_TRACE_INPUTS = 2,        /* after the wait on the preceding grid          */
+  SV_TRACE_FIRST_IDS = 3,     /* producer: first page ids read                 */
+  SV_TRACE_FIRST_MMA = 4,     /* MMA issuer: Q and the first K tile landed     */
+  SV_TRACE_FIRST_S = 5,       /* softmax (row tile 0): first scores ready      */
+  SV_TRACE_LOOP_END = 6,      /* softmax (row tile 0): last P handed over      */
+  SV_TRACE_O_READY = 7,       /* softmax (row tile 0): final O complete        */
+  SV_TRACE_EPILOGUE = 8,      /* output or partial written / parked            */
+  SV_TRACE_MERGE_READY = 9,   /* on-chip merge: all peers published            */
+  SV_TRACE_MERGE_DONE = 10,   /* on-chip merge: own rows merged                */
+  SV_TRACE_EXIT = 11,         /* before TMEM release                           */
+  SV_TRACE_TREE_MASK = 12     /* softmax (row tile 0): ancestor masks built    */
+} sv_trace_event;
+
+sv_status sv_set_trace_buffer(void* buffer, size_t bytes);
 
 /* Reads the error word of a workspace (waits for `stream`), stores it in
  * *code (host) and resets it to zero.  Returns SV_ERR_DEVICE if it was

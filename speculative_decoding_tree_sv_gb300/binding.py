@@ -64,6 +64,8 @@ def load(path: Optional[str] = None):
     lib.sv_status_string.argtypes = [c_int]
     lib.sv_tree_attention_workspace_size.restype = c_int
     lib.sv_tree_attention_workspace_size.argtypes = [P(sv_attn_params), P(c_size_t)]
+    lib.sv_tree_attention_plan.restype = c_int
+    lib.sv_tree_attention_plan.argtypes = [P(sv_attn_params), P(c_int), P(c_int)]
     lib.sv_tree_attention.restype = c_int
     lib.sv_tree_attention.argtypes = [P(sv_attn_params), c_void_p]
     lib.sv_greedy_accept_workspace_size.restype = c_int
@@ -75,6 +77,8 @@ def load(path: Optional[str] = None):
     lib.sv_kv_commit.argtypes = [c_void_p, c_void_p, c_longlong, c_void_p, c_void_p, c_longlong, c_int, c_int,
                                  c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                                  c_int, c_int, c_void_p, c_void_p, c_size_t, c_void_p]
+    lib.sv_set_trace_buffer.restype = c_int
+    lib.sv_set_trace_buffer.argtypes = [c_void_p, c_size_t]
     lib.sv_get_device_error.restype = c_int
     lib.sv_get_device_error.argtypes = [c_void_p, P(c_int), c_void_p]
     if path == _build.library_path():
@@ -152,6 +156,14 @@ def sv_tree_attention_workspace_size(params: sv_attn_params) -> int:
     return int(n.value)
 
 
+def sv_tree_attention_plan(params: sv_attn_params):
+    """(num_splits, split_reduce) the library would launch with."""
+    s, m = c_int(0), c_int(0)
+    _check(load().sv_tree_attention_plan(ctypes.byref(params), ctypes.byref(s), ctypes.byref(m)),
+           "sv_tree_attention_plan")
+    return int(s.value), int(m.value)
+
+
 def sv_tree_attention(params: sv_attn_params, stream=None) -> None:
     _check(load().sv_tree_attention(ctypes.byref(params), _stream(stream)), "sv_tree_attention")
 
@@ -186,6 +198,18 @@ def sv_kv_commit(tree_k, tree_v, tree_layer_stride: int, k_cache, v_cache, cache
                                _ptr(ctx_lens), _ptr(cu_nodes), _ptr(accepted_nodes), _ptr(accept_len), batch,
                                max_depth, num_kv_heads, head_dim, page_size, _ptr(new_ctx_lens),
                                _ptr(workspace), workspace_bytes, _stream(stream)), "sv_kv_commit")
+
+
+TRACE_SLOTS = 16
+TRACE_EVENTS = ["start_ns", "prologue", "inputs", "first_ids", "first_mma", "first_s", "loop_end", "o_ready",
+                "epilogue", "merge_ready", "merge_done", "exit", "tree_mask"]
+
+
+def sv_set_trace_buffer(buffer, nbytes: int = 0) -> None:
+    """Install (or with None remove) the per-CTA phase trace buffer."""
+    if buffer is not None and not nbytes:
+        nbytes = buffer.numel() * buffer.element_size()
+    _check(load().sv_set_trace_buffer(_ptr(buffer), nbytes), "sv_set_trace_buffer")
 
 
 def sv_get_device_error(workspace, stream=None) -> int:

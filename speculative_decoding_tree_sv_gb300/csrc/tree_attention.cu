@@ -92,6 +92,8 @@ struct Params {
   float* part_o;
   float* part_lse;
   int* err;
+  unsigned long long* trace;  // optional per-CTA phase timestamps
+  long long trace_ctas;
   int num_q_heads;
   int group;  // G
   int num_pages;
@@ -121,6 +123,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int G = p.group;
   const bool cluster_mode = p.reduce_mode == kReduceCluster;
+  // phase tracing (diagnostics): no live registers when it is off
+  long long* trace_clk0 = reinterpret_cast<long long*>(smem + C::kOffBar + C::kBarBytes - 8);
+  auto mark = [&](int ev) {
+    if (p.trace != nullptr) {
+      const long long id = blockIdx.x + static_cast<long long>(gridDim.x) *
+                                            (blockIdx.y + static_cast<long long>(gridDim.y) * blockIdx.z);
+      if (id < p.trace_ctas)
+        p.trace[id * kSvTraceSlots + ev] = static_cast<unsigned long long>(clock64() - *trace_clk0);
+    }
+  };
+  if (p.trace != nullptr && threadIdx.x == 0) {
+    *trace_clk0 = clock64();
+    const long long id =
+        blockIdx.x + static_cast<long long>(gridDim.x) * (blockIdx.y + static_cast<long long>(gridDim.y) * blockIdx.z);
+    if (id < p.trace_ctas) p.trace[id * kSvTraceSlots + SV_TRACE_START_NS] = globaltimer_ns();
+  }
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* q_full = bars;
@@ -175,8 +193,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // before anyone can arrive on them remotely
   if (cluster_mode) cluster_sync_all();
   const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) mark(SV_TRACE_PROLOGUE);
   griddep_wait();
   griddep_launch_dependents();
+  if (threadIdx.x == 0) mark(SV_TRACE_INPUTS);
 
   const int n0 = p.cu_nodes[b];
   const int N = p.cu_nodes[b + 1] - n0;
@@ -324,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = mbar_wait(k_full, 0, abort_flag);
         if (ok) {
           tc_fence_after();
+          mark(SV_TRACE_FIRST_MMA);
           for (int t = 0; t < nt; ++t) {
             issue_qk(t, 0);
             umma_commit(s_full + t);
@@ -405,11 +426,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
 
+        if (t == 0 && r == 0 && je == t_all) mark(SV_TRACE_TREE_MASK);
         for (int it = 0; it < ntiles; ++it) {
           const int j = jb + it;
           // warp-uniform outcome: the TMEM loads below are warp-collective
           if (!__all_sync(0xffffffffu, mbar_wait(s_full + t, it & 1, abort_flag))) { ok = false; break; }
           tc_fence_after();
+          if (it == 0 && t == 0 && r == 0) mark(SV_TRACE_FIRST_S);
           uint32_t sr[kBlockN];
   #pragma unroll
           for (int c = 0; c < kBlockN / 32; ++c)
@@ -490,8 +513,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           mbar_arrive(p_full + t);
         }
+        if (t == 0 && r == 0) mark(SV_TRACE_LOOP_END);
 
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_final + t, 0, abort_flag));
+      if (t == 0 && r == 0) mark(SV_TRACE_O_READY);
       if (!ok && lane == 0) {
         report_error(p.err, SV_DEVERR_TIMEOUT);
         *abort_flag = 1;
@@ -506,41 +531,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t orow = static_cast<size_t>(n0 + node) * p.num_q_heads + kh * G + g;
     if (p.reduce_mode == kReduceNone) {
       if (have_o) {
+        uint32_t o[D];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(lane_base + col_o + c * 32, o);
-          tmem_ld_wait();
-          if (row_exists) {
-            uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D + c * 32);
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_base + col_o + c * 32, *reinterpret_cast<uint32_t(*)[32]>(o + c * 32));
+        tmem_ld_wait();
+        if (row_exists) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
-              w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
-              w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
-              w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
-              dst[v] = w;
-            }
+          for (int v = 0; v < D / 8; ++v) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
+            dst[v] = w;
           }
         }
         if (row_exists && p.lse != nullptr) p.lse[orow] = lse2 * kLn2;
       }
+      if (r_cta == 0) mark(SV_TRACE_EPILOGUE);
     } else if (p.reduce_mode == kReduceGlobal) {
       if (have_o) {
         const size_t prow = static_cast<size_t>(split) * p.total_nodes * p.num_q_heads + orow;
+        uint32_t o[D];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(lane_base + col_o + c * 32, o);
-          tmem_ld_wait();
-          if (row_exists) {
-            float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D + c * 32);
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_base + col_o + c * 32, *reinterpret_cast<uint32_t(*)[32]>(o + c * 32));
+        tmem_ld_wait();
+        if (row_exists) {
+          float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D);
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
-                                   __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
-          }
+          for (int v = 0; v < D / 4; ++v)
+            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                 __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
         }
         if (row_exists) p.part_lse[prow] = lse2;
       } else if (row_exists && (t == 0 || tile1)) {
@@ -548,29 +570,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else {
       // ---- on-chip merge across the cluster (one CTA per split)
+      // (trace: SV_TRACE_EPILOGUE marks the parked partial)
+      // The merge buffer lies over the Q/K/V stages: nothing may be written
+      // there before every MMA has finished reading them.  An active group
+      // reaches this barrier only after its final-commit wait; an idle group
+      // (no second row tile) waits here for it.
+      named_barrier(1, 2 * kTileRows);
       float* red_o = reinterpret_cast<float*>(smem + C::kOffRedO);
       float* red_l = reinterpret_cast<float*>(smem + C::kOffRedL);
       if (have_o) {
         float4* dst = reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(red_o) + r_cta * C::kRedStride);
+        uint32_t o[D];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(lane_base + col_o + c * 32, o);
-          tmem_ld_wait();
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_base + col_o + c * 32, *reinterpret_cast<uint32_t(*)[32]>(o + c * 32));
+        tmem_ld_wait();
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[c * 8 + v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
-                                         __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
-        }
+        for (int v = 0; v < D / 4; ++v)
+          dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                               __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
       }
       red_l[r_cta] = lse2;
-      fence_acq_rel_cluster();
+      if (r_cta == 0) mark(SV_TRACE_EPILOGUE);
+      // The CTA barrier orders every softmax thread's writes before the
+      // publishing thread's release (cluster scope, cumulative) arrivals.
       named_barrier(1, 2 * kTileRows);
       const int S = p.num_splits;
       if (threadIdx.x == 4 * 32) {
         for (int rk = 0; rk < S; ++rk) mbar_arrive_cluster(mapa_shared(smem_u32(red_pub), rk));
       }
       if (mbar_wait_cluster(red_pub, 0)) {
+        if (r_cta == 0) mark(SV_TRACE_MERGE_READY);
         constexpr int E = D / 32;  // output elements per lane
         const int rank = static_cast<int>(cluster_ctarank());
         const int rows_cta = min(kCtaRows, rows_total - row0);
@@ -589,20 +618,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           float acc[E];
 #pragma unroll
           for (int e = 0; e < E; ++e) acc[e] = 0.f;
-          for (int s = 0; s < S; ++s) {
-            const float ws = __shfl_sync(0xffffffffu, w, s);
-            if (ws == 0.f) continue;
-            const uint32_t a = mapa_shared(o_base + rr * C::kRedStride + lane * E * 4, s);
-            if constexpr (E == 4) {
-              const float4 v = ld_dsmem_f32x4(a);
-              acc[0] += ws * v.x;
-              acc[1] += ws * v.y;
-              acc[2] += ws * v.z;
-              acc[3] += ws * v.w;
-            } else {
-              const float2 v = ld_dsmem_f32x2(a);
-              acc[0] += ws * v.x;
-              acc[1] += ws * v.y;
+          // issue every peer's load before using any (they are independent)
+          const uint32_t a_loc = o_base + rr * C::kRedStride + lane * E * 4;
+          float4 v4[kMaxClusterSplits];
+#pragma unroll
+          for (int s = 0; s < kMaxClusterSplits; ++s) {
+            if (s < S) {
+              if constexpr (E == 4) {
+                v4[s] = ld_dsmem_f32x4(mapa_shared(a_loc, s));
+              } else {
+                const float2 v = ld_dsmem_f32x2(mapa_shared(a_loc, s));
+                v4[s] = make_float4(v.x, v.y, 0.f, 0.f);
+              }
+            }
+          }
+#pragma unroll
+          for (int s = 0; s < kMaxClusterSplits; ++s) {
+            if (s < S) {
+              const float ws = __shfl_sync(0xffffffffu, w, s);
+              if (ws != 0.f) {  // skipped peers may hold stale, non-finite data
+                acc[0] += ws * v4[s].x;
+                acc[1] += ws * v4[s].y;
+                if constexpr (E == 4) {
+                  acc[2] += ws * v4[s].z;
+                  acc[3] += ws * v4[s].w;
+                }
+              }
             }
           }
           const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
@@ -625,6 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // peers may read our shared memory until every CTA has finished reading
       named_barrier(1, 2 * kTileRows);
+      if (r_cta == 0) mark(SV_TRACE_MERGE_DONE);
       if (threadIdx.x == 4 * 32) {
         for (int rk = 0; rk < S; ++rk) mbar_arrive_cluster(mapa_shared(smem_u32(red_done), rk));
       }
@@ -635,6 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0) mark(SV_TRACE_EXIT);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
@@ -689,6 +732,10 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const float* __restr
 }
 
 // ------------------------------------------------------------------ host
+
+std::mutex g_trace_mu;
+unsigned long long* g_trace = nullptr;
+long long g_trace_ctas = 0;
 
 struct Plan {
   int group;
@@ -811,11 +858,12 @@ void choose_splits(const sv_attn_params* p, int sms, int groups_per_seq, int* sp
     const int act = active_clusters(p->head_dim, s);
     if (act <= 0) return 1e300;
     const long long waves = (units + act - 1) / act;
-    return static_cast<double>(waves) * (static_cast<double>(tiles) / s + c_cta + c_red);
+    return static_cast<double>(waves) * (static_cast<double>((tiles + s - 1) / s) + c_cta + c_red);
   };
   auto cost_global = [&](int s) -> double {
     const long long waves = (units * s + sms - 1) / sms;
-    return static_cast<double>(waves) * (static_cast<double>(tiles) / s + c_cta + c_part) + c_comb + 0.05 * s;
+    return static_cast<double>(waves) * (static_cast<double>((tiles + s - 1) / s) + c_cta + c_part) + c_comb +
+           0.05 * s;
   };
   if (p->num_splits > 0) {
     *splits = p->num_splits;
@@ -919,6 +967,11 @@ sv_status launch(const sv_attn_params* p, const Plan& plan, cudaStream_t stream)
   kp.out = static_cast<__nv_bfloat16*>(p->out);
   kp.lse = p->lse;
   kp.err = reinterpret_cast<int*>(ws);
+  {
+    std::lock_guard<std::mutex> lock(g_trace_mu);
+    kp.trace = g_trace;
+    kp.trace_ctas = g_trace_ctas;
+  }
   const size_t rows = static_cast<size_t>(p->total_nodes) * p->num_q_heads;
   kp.part_o = nullptr;
   kp.part_lse = nullptr;
@@ -964,6 +1017,29 @@ sv_status sv_tree_attention_workspace_size(const sv_attn_params* params, size_t*
   const sv_status st = sv::attn::make_plan(params, &plan);
   if (st != SV_OK) return st;
   *bytes = plan.workspace;
+  return SV_OK;
+}
+
+sv_status sv_set_trace_buffer(void* buffer, size_t bytes) {
+  std::lock_guard<std::mutex> lock(sv::attn::g_trace_mu);
+  if (buffer == nullptr) {
+    sv::attn::g_trace = nullptr;
+    sv::attn::g_trace_ctas = 0;
+    return SV_OK;
+  }
+  if ((reinterpret_cast<uintptr_t>(buffer) & 7u) != 0) return SV_ERR_INVALID_ARG;
+  sv::attn::g_trace = static_cast<unsigned long long*>(buffer);
+  sv::attn::g_trace_ctas = static_cast<long long>(bytes / (kSvTraceSlots * sizeof(unsigned long long)));
+  return SV_OK;
+}
+
+sv_status sv_tree_attention_plan(const sv_attn_params* params, int* num_splits, int* split_reduce) {
+  if (num_splits == nullptr || split_reduce == nullptr) return SV_ERR_INVALID_ARG;
+  sv::attn::Plan plan;
+  const sv_status st = sv::attn::make_plan(params, &plan);
+  if (st != SV_OK) return st;
+  *num_splits = plan.splits;
+  *split_reduce = plan.mode;
   return SV_OK;
 }
 

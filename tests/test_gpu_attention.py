@@ -169,3 +169,14 @@ def test_bad_page_is_reported_not_trapped():
     _, _, err = run_attention(dc, 0, check_error=False)
     assert err == 3
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("nodes", [1, 2, 32])
+@pytest.mark.parametrize("splits", [4, 8])
+def test_single_row_tile_with_on_chip_merge(nodes, splits):
+    # only the first 128-row tile is active: the idle softmax group must not
+    # touch the merge buffer (it overlays the K/V stages) before the MMAs end
+    par = [-1] + list(range(nodes - 1))
+    case = make_case("llama8b_eagle", layers=1, ctx=777, parents_list=[par], with_logits=False)
+    for _ in range(3):
+        _check(case, num_splits=splits, split_reduce=1)
