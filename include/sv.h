@@ -182,6 +182,34 @@ sv_status sv_greedy_accept(const float* logits, int vocab, const int* tokens,
                            int* bonus_token, void* workspace, size_t workspace_bytes,
                            sv_stream_t stream);
 
+/* Greedy acceptance that allocates nothing and takes no workspace.
+ *
+ * No counterpart in the method's description: this is a convenience for
+ * callers that cannot allocate device memory when they verify a tree (an
+ * engine that gave all free memory to its KV pool at start-up, a plugin whose
+ * host framework exposes no allocator, a decode loop that forbids allocation
+ * after warm-up).  Same arguments and results as sv_greedy_accept, without
+ * the workspace; the scratch it needs lives in a fixed array inside this
+ * library's device code, which every GPU that loads the library holds until
+ * the process exits.
+ *   - Limits: batch <= 1024 and total_nodes <= 8192; larger calls return
+ *     SV_ERR_UNSUPPORTED without launching anything.
+ *   - The first call on each device looks up that array's device address (a
+ *     host-side driver query, with the device current); make that first call
+ *     before any stream capture.
+ *   - Every call uses the same array and clears the part it needs at its
+ *     start, so calls that may overlap on the GPU (different streams, or
+ *     different host threads without ordering) race with each other and must
+ *     not be issued.
+ *   - device_error (optional, device int) receives the call's device error
+ *     code (0 if none).
+ * It calls no cudaMalloc, cudaFree or other allocating routine. */
+sv_status sv_greedy_accept_noalloc(const float* logits, int vocab, const int* tokens,
+                                   const int* parents, const int* cu_nodes, int batch,
+                                   int total_nodes, int max_nodes, int max_depth,
+                                   int* argmax_out, int* accept_len, int* accepted_nodes,
+                                   int* bonus_token, int* device_error, sv_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * KV commit of the accepted path, all layers in one launch.
  *

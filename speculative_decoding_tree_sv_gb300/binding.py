@@ -73,6 +73,9 @@ def load(path: Optional[str] = None):
     lib.sv_greedy_accept.restype = c_int
     lib.sv_greedy_accept.argtypes = [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                                      c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
+    lib.sv_greedy_accept_noalloc.restype = c_int
+    lib.sv_greedy_accept_noalloc.argtypes = [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
+                                             c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
     lib.sv_kv_commit.restype = c_int
     lib.sv_kv_commit.argtypes = [c_void_p, c_void_p, c_longlong, c_void_p, c_void_p, c_longlong, c_int, c_int,
                                  c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
@@ -184,6 +187,18 @@ def sv_greedy_accept(logits, vocab: int, tokens, parents, cu_nodes, batch: int, 
                                    total_nodes, max_nodes, max_depth, _ptr(argmax_out), _ptr(accept_len),
                                    _ptr(accepted_nodes), _ptr(bonus_token), _ptr(workspace), workspace_bytes,
                                    _stream(stream)), "sv_greedy_accept")
+
+
+def sv_greedy_accept_noalloc(logits, vocab: int, tokens, parents, cu_nodes, batch: int, total_nodes: int,
+                             max_nodes: int, max_depth: int, argmax_out, accept_len, accepted_nodes, bonus_token,
+                             device_error=None, stream=None) -> None:
+    """Greedy acceptance without a workspace, for callers that cannot
+    allocate device memory; its scratch is a fixed array in the library (see
+    include/sv.h for its limits and for why overlapping calls race)."""
+    _check(load().sv_greedy_accept_noalloc(_ptr(logits), vocab, _ptr(tokens), _ptr(parents), _ptr(cu_nodes),
+                                           batch, total_nodes, max_nodes, max_depth, _ptr(argmax_out),
+                                           _ptr(accept_len), _ptr(accepted_nodes), _ptr(bonus_token),
+                                           _ptr(device_error), _stream(stream)), "sv_greedy_accept_noalloc")
 
 
 def sv_kv_commit(tree_k, tree_v, tree_layer_stride: int, k_cache, v_cache, cache_layer_stride: int,

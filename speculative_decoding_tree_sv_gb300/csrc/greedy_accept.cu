@@ -280,3 +280,76 @@ sv_status sv_greedy_accept(const float* logits, int vocab, const int* tokens, co
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Greedy acceptance without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory at the point where they verify a
+// draft tree: a serving engine that hands all free device memory to its KV
+// pool at start-up, a plugin running inside a host framework that exposes no
+// allocator to it, or a decode loop that forbids allocation after warm-up so
+// that its memory footprint and latency stay fixed.  For them this variant
+// keeps its scratch (the per-row arg-max keys, the per-sequence tickets and
+// the error word) in a fixed array of this library's device module, which
+// every GPU that loads the library holds until the process exits.
+namespace sv {
+namespace acc {
+
+constexpr int kStaticMaxNodes = 8192;
+constexpr int kStaticMaxBatch = 1024;
+constexpr size_t kStaticScratchBytes = kWorkspaceHeader + static_cast<size_t>(kStaticMaxNodes) * 8 +
+                                       static_cast<size_t>(kStaticMaxBatch) * 4 + 512;
+
+static __device__ __align__(256) unsigned char g_accept_scratch[kStaticScratchBytes];
+
+// Device address of the scratch array on the current device.  The first call
+// on each device resolves it (with that device current) and caches it.
+void* static_scratch(sv_status* st) {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *st = SV_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess || p == nullptr) {
+      *st = SV_ERR_CUDA;
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  *st = SV_OK;
+  return addr[dev];
+}
+
+}  // namespace acc
+}  // namespace sv
+
+extern "C" sv_status sv_greedy_accept_noalloc(const float* logits, int vocab, const int* tokens, const int* parents,
+                                              const int* cu_nodes, int batch, int total_nodes, int max_nodes,
+                                              int max_depth, int* argmax_out, int* accept_len, int* accepted_nodes,
+                                              int* bonus_token, int* device_error, sv_stream_t stream) {
+  using namespace sv::acc;
+  if (batch > kStaticMaxBatch || total_nodes > kStaticMaxNodes) return SV_ERR_UNSUPPORTED;
+  if (batch < 1 || total_nodes < 0) return SV_ERR_INVALID_ARG;
+  sv_status st = SV_OK;
+  void* scratch = static_scratch(&st);
+  if (st != SV_OK) return st;
+  size_t used = 0;
+  st = sv_greedy_accept_workspace_size(batch, total_nodes, &used);
+  if (st != SV_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // keys, tickets and the error word must start at zero; the array keeps
+  // whatever the previous call left there
+  if (cudaMemsetAsync(scratch, 0, used, s) != cudaSuccess) return SV_ERR_CUDA;
+  st = sv_greedy_accept(logits, vocab, tokens, parents, cu_nodes, batch, total_nodes, max_nodes, max_depth,
+                        argmax_out, accept_len, accepted_nodes, bonus_token, scratch, kStaticScratchBytes, stream);
+  if (st != SV_OK) return st;
+  if (device_error != nullptr &&
+      cudaMemcpyAsync(device_error, scratch, sizeof(int), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return SV_ERR_CUDA;
+  return SV_OK;
+}
