@@ -84,6 +84,23 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_traffic(config: str):
+    """DRAM bytes per attention launch from the committed ncu record, or None
+    when the kernel source changed since those counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "speculative_decoding_tree_sv_gb300", "csrc", "tree_attention.cu")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(config)
+    if not rec:
+        return None
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    return rec["dram_bytes_per_launch"] if h == rec.get("kernel_source_sha256_16") else None
+
+
 class ClockSampler:
     """Samples SM clocks and throttle reasons with nvidia-smi while running."""
 
@@ -362,11 +379,7 @@ def run_gpu(args):
     attn_launch_s = ms_attn * 1e-3 / (args.steps * c.num_layers)
     achieved = bytes_launch / attn_launch_s / 1e9
     peak, peak_kind = measured_peaks()
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", f"traffic_{args.config}.json")
-    if os.path.exists(tpath):
-        with open(tpath) as f:
-            traffic = json.load(f).get("dram_bytes_per_launch")
+    traffic = measured_traffic(args.config)
 
     # end to end through the public API with host buffers: pinned H2D of the
     # step's inputs, the step, D2H of the results; captured like the step.
