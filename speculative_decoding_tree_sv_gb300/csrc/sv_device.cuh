@@ -146,6 +146,24 @@ __device__ __forceinline__ float2 ld_dsmem_f32x2(uint32_t addr) {
   return v;
 }
 
+// Make this thread's generic-proxy shared-memory writes visible to the
+// async proxy (bulk copies, TMA) that reads them next.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to a
+// peer CTA's shared memory; completes as transaction bytes on the peer's
+// mbarrier (both peer addresses are shared::cluster addresses).
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                                  uint32_t mbar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(src_cta), "r"(bytes), "r"(mbar_cluster)
+      : "memory");
+}
+
 // Programmatic dependent launch: wait for the grids this one depends on
 // (their memory is visible afterwards), and allow dependents to launch.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

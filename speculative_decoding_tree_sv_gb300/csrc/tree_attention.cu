@@ -23,13 +23,13 @@
 //     warps 4-7 and 8-11 run the softmax of row tiles 0 and 1.  The MMA
 //     issue order S0 S1 | PV0 S0' | PV1 S1' ... keeps the tensor core busy
 //     while the two softmax groups alternate.
-//   * KV splits are merged one of two ways.  On chip: the splits of one
-//     (sequence, head group) form a thread-block cluster; each CTA parks
-//     O / l and log2-sum-exp in its shared memory and every CTA merges a
-//     slice of the rows by reading its peers' shared memory (DSMEM), with
-//     mbarrier handshakes whose waits are bounded.  Through global memory:
-//     each split writes a partial that a second kernel merges (for very long
-//     contexts, where more splits than fit in co-resident clusters pay off).
+//   * KV splits are merged one of two ways.  Inside a cluster: the splits of
+//     one (sequence, head group) form a thread-block cluster, so they are
+//     co-resident; each writes its partial (O / l, log2-sum-exp) to the
+//     workspace, signals its peers' mbarriers, waits for theirs (bounded)
+//     and merges a slice of the rows from L2.  With a second kernel: for
+//     very long contexts, where more splits than fit in co-resident clusters
+//     pay off, the splits write partials that a combine kernel merges.
 //   * Launches allow programmatic dependent launch: the prologue (barriers,
 //     TMEM, descriptor prefetch) runs before the wait on the previous grid.
 #include <math.h>
@@ -72,12 +72,6 @@ struct Cfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128;
   static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
-  // on-chip split merge: per-row O / l (fp32, padded rows) and log2-sum-exp,
-  // parked over the Q/K/V area once the main loop is done
-  static constexpr uint32_t kRedStride = D * 4 + 16;
-  static constexpr uint32_t kOffRedO = 0;
-  static constexpr uint32_t kOffRedL = kOffRedO + kCtaRows * kRedStride;
-  static_assert(kOffRedL + kCtaRows * 4 <= kOffBar, "merge buffer must fit below the barriers");
 };
 
 struct Params {
@@ -150,9 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_full + 2;     // [2]
   uint64_t* o_final = p_full + 2;    // [2]
   uint64_t* drain = o_final + 2;
-  uint64_t* red_pub = drain + 1;     // cluster merge: peers published
-  uint64_t* red_done = red_pub + 1;  // cluster merge: peers finished reading
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_done + 1);
+  uint64_t* published = drain + 1;   // cluster merge: every peer's partial is in the workspace
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(published + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* never_set = abort_flag + 1;  // drains wait on copies even after an abort
 
@@ -171,8 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(o_final + t, 1);
     }
     mbar_init(drain, 1);
-    mbar_init(red_pub, p.num_splits);
-    mbar_init(red_done, p.num_splits);
+    mbar_init(published, p.num_splits);
     *abort_flag = 0;
     *never_set = 0;
     fence_mbar_init();
@@ -463,11 +455,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float tmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
           const float m_new = fmaxf(m_run, tmax);
-          if (m_new > m_run + kRescaleThreshold) {
-            if (it > 0) {
-              // O already holds earlier tiles (their PV finished before this S
-              // was committed): rescale it and the running sum.
-              const float f = ex2(m_run - m_new);
+          const bool grow = m_new > m_run + kRescaleThreshold;
+          // The O rescale reads and writes TMEM with warp-collective
+          // instructions: the whole warp takes it when any row needs it
+          // (rows that do not are scaled by 1).
+          if (it > 0 && __any_sync(0xffffffffu, grow)) {
+            // O already holds earlier tiles (their PV finished before this S
+            // was committed): rescale it and the running sum.
+            {
+              const float f = grow ? ex2(m_run - m_new) : 1.f;
               l_run *= f;
               const uint64_t f2 = f2_pack(f, f);
               uint32_t o[32];
@@ -485,8 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               tmem_st_wait();
             }
-            m_run = m_new;
           }
+          if (grow) m_run = m_new;
           const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
           // p = 2^(s * scale_log2 - m), packed two at a time
           const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
@@ -569,45 +565,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.part_lse[static_cast<size_t>(split) * p.total_nodes * p.num_q_heads + orow] = -INFINITY;
       }
     } else {
-      // ---- on-chip merge across the cluster (one CTA per split)
-      // (trace: SV_TRACE_EPILOGUE marks the parked partial)
-      // The merge buffer lies over the Q/K/V stages: nothing may be written
-      // there before every MMA has finished reading them.  An active group
-      // reaches this barrier only after its final-commit wait; an idle group
-      // (no second row tile) waits here for it.
-      named_barrier(1, 2 * kTileRows);
-      float* red_o = reinterpret_cast<float*>(smem + C::kOffRedO);
-      float* red_l = reinterpret_cast<float*>(smem + C::kOffRedL);
-      if (have_o) {
-        float4* dst = reinterpret_cast<float4*>(reinterpret_cast<uint8_t*>(red_o) + r_cta * C::kRedStride);
+      // ---- merge inside the cluster (one CTA per split, co-resident)
+      // Each CTA writes its partial rows (O / l and log2-sum-exp, fp32) to
+      // the workspace, tells its peers through their mbarriers (release at
+      // cluster scope), waits until every peer has done the same (bounded),
+      // then merges its own slice of the rows from the peers' partials,
+      // which sit in L2.  Global memory outlives the CTAs: no exit handshake.
+      const int S = p.num_splits;
+      const int rank = static_cast<int>(cluster_ctarank());
+      const size_t prow = static_cast<size_t>(split) * p.total_nodes * p.num_q_heads + orow;
+      if (have_o) {  // warp-uniform: the TMEM read is warp-collective
         uint32_t o[D];
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_base + col_o + c * 32, *reinterpret_cast<uint32_t(*)[32]>(o + c * 32));
         tmem_ld_wait();
+        if (row_exists) {
+          float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D);
 #pragma unroll
-        for (int v = 0; v < D / 4; ++v)
-          dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
-                               __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+          for (int v = 0; v < D / 4; ++v)
+            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                 __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+        }
       }
-      red_l[r_cta] = lse2;
+      if (row_exists && (t == 0 || tile1)) p.part_lse[prow] = lse2;
       if (r_cta == 0) mark(SV_TRACE_EPILOGUE);
-      // The CTA barrier orders every softmax thread's writes before the
-      // publishing thread's release (cluster scope, cumulative) arrivals.
       named_barrier(1, 2 * kTileRows);
-      const int S = p.num_splits;
       if (threadIdx.x == 4 * 32) {
-        for (int rk = 0; rk < S; ++rk) mbar_arrive_cluster(mapa_shared(smem_u32(red_pub), rk));
+        for (int rk = 0; rk < S; ++rk) mbar_arrive_cluster(mapa_shared(smem_u32(published), rk));
       }
-      if (mbar_wait_cluster(red_pub, 0)) {
+      if (mbar_wait_cluster(published, 0)) {
         if (r_cta == 0) mark(SV_TRACE_MERGE_READY);
         constexpr int E = D / 32;  // output elements per lane
-        const int rank = static_cast<int>(cluster_ctarank());
         const int rows_cta = min(kCtaRows, rows_total - row0);
         const int slice = (rows_cta + S - 1) / S;
         const int lo = rank * slice, hi = min(rows_cta, lo + slice);
-        const uint32_t o_base = smem_u32(red_o), l_base = smem_u32(red_l);
+        const size_t split_stride = static_cast<size_t>(p.total_nodes) * p.num_q_heads;
         for (int rr = lo + (warp - 4); rr < hi; rr += 8) {
-          const float ls = (lane < S) ? ld_dsmem_f32(mapa_shared(l_base + rr * 4, lane)) : -INFINITY;
+          const int grow = row0 + rr;
+          const int gnode = grow / G;
+          const size_t out_row = static_cast<size_t>(n0 + gnode) * p.num_q_heads + kh * G + (grow - gnode * G);
+          const float ls = (lane < S) ? __ldcg(p.part_lse + lane * split_stride + out_row) : -INFINITY;
           float mx = ls;
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -615,28 +612,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           float wsum = w;
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-          float acc[E];
-#pragma unroll
-          for (int e = 0; e < E; ++e) acc[e] = 0.f;
-          // issue every peer's load before using any (they are independent)
-          const uint32_t a_loc = o_base + rr * C::kRedStride + lane * E * 4;
+          // issue every peer's load before using any
           float4 v4[kMaxClusterSplits];
 #pragma unroll
           for (int s = 0; s < kMaxClusterSplits; ++s) {
             if (s < S) {
+              const float* src = p.part_o + (s * split_stride + out_row) * D + lane * E;
               if constexpr (E == 4) {
-                v4[s] = ld_dsmem_f32x4(mapa_shared(a_loc, s));
+                v4[s] = __ldcg(reinterpret_cast<const float4*>(src));
               } else {
-                const float2 v = ld_dsmem_f32x2(mapa_shared(a_loc, s));
+                const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
                 v4[s] = make_float4(v.x, v.y, 0.f, 0.f);
               }
             }
           }
+          float acc[E];
+#pragma unroll
+          for (int e = 0; e < E; ++e) acc[e] = 0.f;
 #pragma unroll
           for (int s = 0; s < kMaxClusterSplits; ++s) {
             if (s < S) {
               const float ws = __shfl_sync(0xffffffffu, w, s);
-              if (ws != 0.f) {  // skipped peers may hold stale, non-finite data
+              if (ws != 0.f) {  // skipped peers may hold stale, non-finite rows
                 acc[0] += ws * v4[s].x;
                 acc[1] += ws * v4[s].y;
                 if constexpr (E == 4) {
@@ -647,9 +644,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
-          const int grow = row0 + rr;
-          const int gnode = grow / G;
-          const size_t out_row = static_cast<size_t>(n0 + gnode) * p.num_q_heads + kh * G + (grow - gnode * G);
           __nv_bfloat16* dst = p.out + out_row * D + lane * E;
           if constexpr (E == 4) {
             uint2 v;
@@ -664,13 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (lane == 0) {
         report_error(p.err, SV_DEVERR_TIMEOUT);
       }
-      // peers may read our shared memory until every CTA has finished reading
-      named_barrier(1, 2 * kTileRows);
       if (r_cta == 0) mark(SV_TRACE_MERGE_DONE);
-      if (threadIdx.x == 4 * 32) {
-        for (int rk = 0; rk < S; ++rk) mbar_arrive_cluster(mapa_shared(smem_u32(red_done), rk));
-      }
-      if (!mbar_wait_cluster(red_done, 0) && lane == 0) report_error(p.err, SV_DEVERR_TIMEOUT);
     }
   }
   }  // row group exists
@@ -910,7 +898,7 @@ sv_status make_plan(const sv_attn_params* p, Plan* plan) {
   }
   choose_splits(p, sms, plan->groups_per_seq, &plan->splits, &plan->mode);
   size_t ws = kWorkspaceHeader;
-  if (plan->mode == kReduceGlobal) {
+  if (plan->mode != kReduceNone) {
     const size_t rows = static_cast<size_t>(p->total_nodes) * p->num_q_heads;
     ws += align_up(static_cast<size_t>(plan->splits) * rows * p->head_dim * sizeof(float), 256);
     ws += align_up(static_cast<size_t>(plan->splits) * rows * sizeof(float), 256);
@@ -975,7 +963,7 @@ sv_status launch(const sv_attn_params* p, const Plan& plan, cudaStream_t stream)
   const size_t rows = static_cast<size_t>(p->total_nodes) * p->num_q_heads;
   kp.part_o = nullptr;
   kp.part_lse = nullptr;
-  if (plan.mode == kReduceGlobal) {
+  if (plan.mode != kReduceNone) {
     kp.part_o = reinterpret_cast<float*>(ws + kWorkspaceHeader);
     kp.part_lse = reinterpret_cast<float*>(
         ws + kWorkspaceHeader + align_up(static_cast<size_t>(plan.splits) * rows * D * sizeof(float), 256));
