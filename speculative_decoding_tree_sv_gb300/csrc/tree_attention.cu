@@ -72,6 +72,11 @@ struct Cfg {
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128;
   static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
+  // epilogue staging of output rows (one padded row per softmax thread),
+  // over the Q/K/V stages once every MMA is done
+  static constexpr uint32_t kStageStride = D * 4 + 16;
+  static constexpr uint32_t kOffStage = 0;
+  static_assert(kOffStage + 2 * kTileRows * kStageStride <= kOffBar, "staging must fit below the barriers");
 };
 
 struct Params {
@@ -83,8 +88,8 @@ struct Params {
   const int* cu_kv_pages;
   __nv_bfloat16* out;
   float* lse;
-  float* part_o;
-  float* part_lse;
+  __nv_bfloat16* part_o;  // split partials O / l (bf16), [splits][T * Hq][D]
+  float* part_lse;        // split partials log2-sum-exp, [splits][T * Hq]
   int* err;
   unsigned long long* trace;  // optional per-CTA phase timestamps
   long long trace_ctas;
@@ -525,69 +530,63 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
     const float lse2 = (have_o && l_run > 0.f) ? m_run + log2f(l_run) : -INFINITY;
     const size_t orow = static_cast<size_t>(n0 + node) * p.num_q_heads + kh * G + g;
-    if (p.reduce_mode == kReduceNone) {
-      if (have_o) {
-        uint32_t o[D];
+    // Output rows leave through shared memory: each thread parks its row
+    // (one TMEM lane) in a padded staging row over the dead Q/K/V stages
+    // (every MMA finished before o_final fired), then the warp writes whole
+    // rows, lane l moving chunk l, so global stores are coalesced.
+    const bool partial_out = p.reduce_mode != kReduceNone;
+    if (have_o) {
+      uint32_t o[D];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_base + col_o + c * 32, *reinterpret_cast<uint32_t(*)[32]>(o + c * 32));
-        tmem_ld_wait();
-        if (row_exists) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D);
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_base + col_o + c * 32, *reinterpret_cast<uint32_t(*)[32]>(o + c * 32));
+      tmem_ld_wait();
+      uint8_t* stage = smem + C::kOffStage + (warp - 4) * 32 * C::kStageStride;
+      uint8_t* mine = stage + lane * C::kStageStride;
 #pragma unroll
-          for (int v = 0; v < D / 8; ++v) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
-            dst[v] = w;
-          }
-        }
-        if (row_exists && p.lse != nullptr) p.lse[orow] = lse2 * kLn2;
+      for (int v = 0; v < D / 8; ++v) {
+        uint4 w;
+        w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
+        w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
+        w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
+        w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
+        reinterpret_cast<uint4*>(mine)[v] = w;
       }
+      __syncwarp();
+      // rows of D bf16 = D / 8 16-byte chunks; the warp stores 256 / D rows per
+      // instruction
+      constexpr int kChunks = D / 8;
+      constexpr int kRowsPerPass = 32 / kChunks;
+      const int wrow0 = row0 + t * kTileRows + qw * 32;
+      const int nrows = min(32, rows_total - wrow0);
+      const size_t split_base = partial_out ? static_cast<size_t>(split) * p.total_nodes * p.num_q_heads : 0;
+      const long long my_out_row = static_cast<long long>(split_base + orow);  // this lane's row
+      __nv_bfloat16* const base = partial_out ? p.part_o : p.out;
+      for (int rb = 0; rb < nrows; rb += kRowsPerPass) {
+        const int rr = rb + lane / kChunks;
+        const long long grow_out = __shfl_sync(0xffffffffu, my_out_row, min(rr, 31));
+        if (rr < nrows)
+          reinterpret_cast<uint4*>(base + grow_out * D)[lane % kChunks] =
+              reinterpret_cast<const uint4*>(stage + rr * C::kStageStride)[lane % kChunks];
+      }
+    }
+    if (p.reduce_mode == kReduceNone) {
+      if (have_o && row_exists && p.lse != nullptr) p.lse[orow] = lse2 * kLn2;
       if (r_cta == 0) mark(SV_TRACE_EPILOGUE);
     } else if (p.reduce_mode == kReduceGlobal) {
-      if (have_o) {
-        const size_t prow = static_cast<size_t>(split) * p.total_nodes * p.num_q_heads + orow;
-        uint32_t o[D];
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_base + col_o + c * 32, *reinterpret_cast<uint32_t(*)[32]>(o + c * 32));
-        tmem_ld_wait();
-        if (row_exists) {
-          float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D);
-#pragma unroll
-          for (int v = 0; v < D / 4; ++v)
-            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
-                                 __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
-        }
-        if (row_exists) p.part_lse[prow] = lse2;
-      } else if (row_exists && (t == 0 || tile1)) {
-        p.part_lse[static_cast<size_t>(split) * p.total_nodes * p.num_q_heads + orow] = -INFINITY;
-      }
+      if (row_exists && (t == 0 || tile1))
+        p.part_lse[static_cast<size_t>(split) * p.total_nodes * p.num_q_heads + orow] = lse2;
     } else {
       // ---- merge inside the cluster (one CTA per split, co-resident)
-      // Each CTA writes its partial rows (O / l and log2-sum-exp, fp32) to
-      // the workspace, tells its peers through their mbarriers (release at
-      // cluster scope), waits until every peer has done the same (bounded),
-      // then merges its own slice of the rows from the peers' partials,
-      // which sit in L2.  Global memory outlives the CTAs: no exit handshake.
+      // Each CTA has written its partial rows (O / l and log2-sum-exp, fp32)
+      // to the workspace; it tells its peers through their mbarriers
+      // (release at cluster scope), waits until every peer has done the same
+      // (bounded), then merges its own slice of the rows from the peers'
+      // partials, which sit in L2.  Global memory outlives the CTAs: no exit
+      // handshake is needed.
       const int S = p.num_splits;
       const int rank = static_cast<int>(cluster_ctarank());
-      const size_t prow = static_cast<size_t>(split) * p.total_nodes * p.num_q_heads + orow;
-      if (have_o) {  // warp-uniform: the TMEM read is warp-collective
-        uint32_t o[D];
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_base + col_o + c * 32, *reinterpret_cast<uint32_t(*)[32]>(o + c * 32));
-        tmem_ld_wait();
-        if (row_exists) {
-          float4* dst = reinterpret_cast<float4*>(p.part_o + prow * D);
-#pragma unroll
-          for (int v = 0; v < D / 4; ++v)
-            dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
-                                 __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
-        }
-      }
-      if (row_exists && (t == 0 || tile1)) p.part_lse[prow] = lse2;
+      const size_t split_stride = static_cast<size_t>(p.total_nodes) * p.num_q_heads;
+      if (row_exists && (t == 0 || tile1)) p.part_lse[static_cast<size_t>(split) * split_stride + orow] = lse2;
       if (r_cta == 0) mark(SV_TRACE_EPILOGUE);
       named_barrier(1, 2 * kTileRows);
       if (threadIdx.x == 4 * 32) {
@@ -596,64 +595,75 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (mbar_wait_cluster(published, 0)) {
         if (r_cta == 0) mark(SV_TRACE_MERGE_READY);
         constexpr int E = D / 32;  // output elements per lane
+        constexpr int R = 2;       // rows merged together (their loads overlap)
         const int rows_cta = min(kCtaRows, rows_total - row0);
         const int slice = (rows_cta + S - 1) / S;
         const int lo = rank * slice, hi = min(rows_cta, lo + slice);
-        const size_t split_stride = static_cast<size_t>(p.total_nodes) * p.num_q_heads;
-        for (int rr = lo + (warp - 4); rr < hi; rr += 8) {
-          const int grow = row0 + rr;
-          const int gnode = grow / G;
-          const size_t out_row = static_cast<size_t>(n0 + gnode) * p.num_q_heads + kh * G + (grow - gnode * G);
-          const float ls = (lane < S) ? __ldcg(p.part_lse + lane * split_stride + out_row) : -INFINITY;
-          float mx = ls;
+        for (int rb = lo + (warp - 4) * R; rb < hi; rb += 8 * R) {
+          size_t out_row[R];
+          float ls[R];
+          float4 v4[R][kMaxClusterSplits];
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-          const float w = (ls == -INFINITY) ? 0.f : ex2(ls - mx);
-          float wsum = w;
+          for (int q = 0; q < R; ++q) {
+            const int rr = min(rb + q, hi - 1);  // a duplicate row is merged twice, harmlessly
+            const int grow = row0 + rr;
+            const int gnode = grow / G;
+            out_row[q] = static_cast<size_t>(n0 + gnode) * p.num_q_heads + kh * G + (grow - gnode * G);
+            ls[q] = (lane < S) ? __ldcg(p.part_lse + lane * split_stride + out_row[q]) : -INFINITY;
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-          // issue every peer's load before using any
-          float4 v4[kMaxClusterSplits];
-#pragma unroll
-          for (int s = 0; s < kMaxClusterSplits; ++s) {
-            if (s < S) {
-              const float* src = p.part_o + (s * split_stride + out_row) * D + lane * E;
-              if constexpr (E == 4) {
-                v4[s] = __ldcg(reinterpret_cast<const float4*>(src));
-              } else {
-                const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
-                v4[s] = make_float4(v.x, v.y, 0.f, 0.f);
-              }
-            }
-          }
-          float acc[E];
-#pragma unroll
-          for (int e = 0; e < E; ++e) acc[e] = 0.f;
-#pragma unroll
-          for (int s = 0; s < kMaxClusterSplits; ++s) {
-            if (s < S) {
-              const float ws = __shfl_sync(0xffffffffu, w, s);
-              if (ws != 0.f) {  // skipped peers may hold stale, non-finite rows
-                acc[0] += ws * v4[s].x;
-                acc[1] += ws * v4[s].y;
+            for (int s = 0; s < kMaxClusterSplits; ++s) {
+              if (s < S) {
+                const __nv_bfloat16* src = p.part_o + (s * split_stride + out_row[q]) * D + lane * E;
                 if constexpr (E == 4) {
-                  acc[2] += ws * v4[s].z;
-                  acc[3] += ws * v4[s].w;
+                  const uint2 v = __ldcg(reinterpret_cast<const uint2*>(src));
+                  v4[q][s] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
+                                         __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+                } else {
+                  const uint32_t v = __ldcg(reinterpret_cast<const unsigned int*>(src));
+                  v4[q][s] = make_float4(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u), 0.f, 0.f);
                 }
               }
             }
           }
-          const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
-          __nv_bfloat16* dst = p.out + out_row * D + lane * E;
-          if constexpr (E == 4) {
-            uint2 v;
-            v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-            v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-            *reinterpret_cast<uint2*>(dst) = v;
-          } else {
-            *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+#pragma unroll
+          for (int q = 0; q < R; ++q) {
+            if (rb + q >= hi) break;
+            float mx = ls[q];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            const float w = (ls[q] == -INFINITY) ? 0.f : ex2(ls[q] - mx);
+            float wsum = w;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+            float acc[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll
+            for (int s = 0; s < kMaxClusterSplits; ++s) {
+              if (s < S) {
+                const float ws = __shfl_sync(0xffffffffu, w, s);
+                if (ws != 0.f) {  // skipped peers may hold stale, non-finite rows
+                  acc[0] += ws * v4[q][s].x;
+                  acc[1] += ws * v4[q][s].y;
+                  if constexpr (E == 4) {
+                    acc[2] += ws * v4[q][s].z;
+                    acc[3] += ws * v4[q][s].w;
+                  }
+                }
+              }
+            }
+            const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
+            __nv_bfloat16* dst = p.out + out_row[q] * D + lane * E;
+            if constexpr (E == 4) {
+              uint2 v;
+              v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+              v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+              *reinterpret_cast<uint2*>(dst) = v;
+            } else {
+              *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+            }
+            if (lane == 0 && p.lse != nullptr) p.lse[out_row[q]] = (mx + log2f(wsum)) * kLn2;
           }
-          if (lane == 0 && p.lse != nullptr) p.lse[out_row] = (mx + log2f(wsum)) * kLn2;
         }
       } else if (lane == 0) {
         report_error(p.err, SV_DEVERR_TIMEOUT);
@@ -674,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Merge split partials: O = sum_s w_s O_s / sum_s w_s, w_s = 2^(lse_s - max).
 template <int D>
-__global__ void __launch_bounds__(256) split_combine_kernel(const float* __restrict__ part_o,
+__global__ void __launch_bounds__(256) split_combine_kernel(const __nv_bfloat16* __restrict__ part_o,
                                                             const float* __restrict__ part_lse,
                                                             __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
                                                             int rows, int splits) {
@@ -693,17 +703,17 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const float* __restr
     if (ls == -INFINITY) continue;
     const float w = ex2(ls - mx);
     wsum += w;
-    const float* src = part_o + (static_cast<size_t>(s) * rows + row) * D + lane * E;
+    const __nv_bfloat16* src = part_o + (static_cast<size_t>(s) * rows + row) * D + lane * E;
     if constexpr (E == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(src);
-      acc[0] += w * v.x;
-      acc[1] += w * v.y;
-      acc[2] += w * v.z;
-      acc[3] += w * v.w;
+      const uint2 v = *reinterpret_cast<const uint2*>(src);
+      acc[0] += w * __uint_as_float(v.x << 16);
+      acc[1] += w * __uint_as_float(v.x & 0xFFFF0000u);
+      acc[2] += w * __uint_as_float(v.y << 16);
+      acc[3] += w * __uint_as_float(v.y & 0xFFFF0000u);
     } else {
-      const float2 v = *reinterpret_cast<const float2*>(src);
-      acc[0] += w * v.x;
-      acc[1] += w * v.y;
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(src);
+      acc[0] += w * __uint_as_float(v << 16);
+      acc[1] += w * __uint_as_float(v & 0xFFFF0000u);
     }
   }
   const float inv = 1.f / wsum;
@@ -841,7 +851,9 @@ void choose_splits(const sv_attn_params* p, int sms, int groups_per_seq, int* sp
   const long long units = static_cast<long long>(p->batch) * p->num_kv_heads * groups_per_seq;
   const int pages = p->kv_pages ? p->max_kv_pages : p->max_pages_per_seq;
   const int tiles = (pages + kPagesPerTile - 1) / kPagesPerTile + 1;
-  const double c_cta = 1.5, c_red = 0.75, c_part = 1.0, c_comb = 2.0;
+  // merge costs measured on GB300 (in tiles of work): the in-cluster merge is
+  // latency-bound (~5 us); partial writes ~1 tile; the combine kernel ~2
+  const double c_cta = 1.5, c_red = 4.0, c_part = 1.0, c_comb = 2.0;
   auto cost_cluster = [&](int s) -> double {
     const int act = active_clusters(p->head_dim, s);
     if (act <= 0) return 1e300;
@@ -900,8 +912,8 @@ sv_status make_plan(const sv_attn_params* p, Plan* plan) {
   size_t ws = kWorkspaceHeader;
   if (plan->mode != kReduceNone) {
     const size_t rows = static_cast<size_t>(p->total_nodes) * p->num_q_heads;
-    ws += align_up(static_cast<size_t>(plan->splits) * rows * p->head_dim * sizeof(float), 256);
-    ws += align_up(static_cast<size_t>(plan->splits) * rows * sizeof(float), 256);
+    ws += align_up(static_cast<size_t>(plan->splits) * rows * p->head_dim * 2, 256);  // bf16 O / l
+    ws += align_up(static_cast<size_t>(plan->splits) * rows * sizeof(float), 256);   // log2-sum-exp
   }
   plan->workspace = ws;
   return SV_OK;
@@ -964,9 +976,9 @@ sv_status launch(const sv_attn_params* p, const Plan& plan, cudaStream_t stream)
   kp.part_o = nullptr;
   kp.part_lse = nullptr;
   if (plan.mode != kReduceNone) {
-    kp.part_o = reinterpret_cast<float*>(ws + kWorkspaceHeader);
-    kp.part_lse = reinterpret_cast<float*>(
-        ws + kWorkspaceHeader + align_up(static_cast<size_t>(plan.splits) * rows * D * sizeof(float), 256));
+    kp.part_o = reinterpret_cast<__nv_bfloat16*>(ws + kWorkspaceHeader);
+    kp.part_lse = reinterpret_cast<float*>(ws + kWorkspaceHeader +
+                                           align_up(static_cast<size_t>(plan.splits) * rows * D * 2, 256));
   }
   kp.num_q_heads = p->num_q_heads;
   kp.group = G;
