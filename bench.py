@@ -175,7 +175,7 @@ def build_case(name: str, seed_offset: int = 0):
 class GpuStep:
     """Device-resident inputs and the library calls of one verify step."""
 
-    def __init__(self, case, partial: bool, dev: str):
+    def __init__(self, case, partial: bool, dev: str, flags: int = 0):
         import torch
 
         from speculative_decoding_tree_sv_gb300 import binding
@@ -214,7 +214,7 @@ class GpuStep:
                 v_cache=self.v_cache[l], block_table=self.block_table, ctx_lens=self.ctx_lens,
                 cu_nodes=self.cu_nodes, parents=self.parents, out=self.out[l], total_nodes=self.T,
                 max_nodes=c.max_nodes, kv_pages=self.kv_pages, cu_kv_pages=self.cu_kv_pages,
-                max_kv_pages=self.max_kv_pages)
+                max_kv_pages=self.max_kv_pages, flags=flags)
             ws_bytes = max(ws_bytes, binding.sv_tree_attention_workspace_size(p))
             self.params.append(p)
         self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
@@ -344,6 +344,7 @@ def run_reference(args):
 def run_gpu(args):
     import torch
 
+    from speculative_decoding_tree_sv_gb300 import binding
     from speculative_decoding_tree_sv_gb300 import build as _build
     from speculative_decoding_tree_sv_gb300 import cost
 
@@ -355,7 +356,8 @@ def run_gpu(args):
     dev = f"cuda:{local}"
     _build.build()
     case, partial = build_case(args.config)
-    st = GpuStep(case, partial, dev)
+    flags = binding.SV_ATTN_EARLY_CONTEXT if args.early_context else 0
+    st = GpuStep(case, partial, dev, flags=flags)
     c = case
     nodes_per_step = c.total_nodes * c.num_layers
 
@@ -419,7 +421,7 @@ def run_gpu(args):
             "config": {"workload": WORKLOADS[args.config], "layers": c.num_layers, "batch": c.batch,
                        "total_nodes": c.total_nodes, "kv_splits": st.splits,
                        "split_merge": ["none", "on-chip cluster", "global partials"][st.split_reduce],
-                       "cuda_graph": True,
+                       "cuda_graph": True, "early_context": bool(flags),
                        "l2": "inputs larger than L2 (distinct KV per layer, %.0f MB per step)"
                              % (sum(ctx_keys) * 4 * c.num_kv_heads * c.head_dim * c.num_layers / 1e6),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -447,6 +449,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["sv", "reference"], default="sv")
     ap.add_argument("--config", choices=sorted(WORKLOADS), default="llama8b_eagle")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--early-context", action="store_true",
+                    help="launch attention with SV_ATTN_EARLY_CONTEXT")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -93,6 +93,21 @@ const char* sv_status_string(sv_status status);
  * ancestors of i or i itself.  The root is not part of L_b.  Q and K arrive
  * with positional encoding already applied.
  * ---------------------------------------------------------------------- */
+/* Options of sv_tree_attention (sv_attn_params.flags).
+ *
+ * SV_ATTN_EARLY_CONTEXT: the kernel is launched as a programmatic dependent
+ * of the kernel before it in the stream, so it may start while that kernel
+ * is still running; by default it reads nothing before that kernel has
+ * finished.  With this flag it already reads the page tables, ctx_lens,
+ * cu_nodes, parents, the partial page list and the context K/V pages (cache
+ * slots below ctx_lens[b]) in that window, and waits only before it reads Q
+ * and the tree's K/V and before it writes anything.  Set it when none of
+ * those inputs is written by a preceding kernel that signals early
+ * completion (griddepcontrol.launch_dependents) before writing them; the
+ * kernels of this library never write them.  Consecutive layers then
+ * overlap one layer's context loads with the previous layer's tail. */
+enum sv_attn_flags { SV_ATTN_EARLY_CONTEXT = 1 };
+
 typedef struct sv_attn_params {
   /* shapes (host values) */
   int batch;              /* B >= 1                                          */
@@ -112,6 +127,7 @@ typedef struct sv_attn_params {
                              <= 16), 2 = through workspace partials and a
                              second kernel                                   */
   float sm_scale;         /* softmax scale; <= 0 selects 1/sqrt(D)           */
+  int flags;              /* bitwise OR of sv_attn_flags, 0 for none         */
 
   /* tensors */
   const void* q;          /* bf16 [T, Hq, D]                                 */

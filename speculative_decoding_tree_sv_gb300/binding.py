@@ -20,6 +20,7 @@ from . import build as _build
 SV_OK = 0
 STATUS_NAMES = {0: "SV_OK", 1: "SV_ERR_INVALID_ARG", 2: "SV_ERR_UNSUPPORTED", 3: "SV_ERR_CUDA",
                 4: "SV_ERR_WORKSPACE", 5: "SV_ERR_DEVICE", 6: "SV_ERR_TIMEOUT"}
+SV_ATTN_EARLY_CONTEXT = 1
 DEVICE_ERRORS = {0: "none", 1: "timeout", 2: "bad parent", 3: "bad page", 4: "bad path", 5: "depth",
                  6: "bad tree"}
 
@@ -35,7 +36,7 @@ class sv_attn_params(ctypes.Structure):
         ("batch", c_int), ("num_q_heads", c_int), ("num_kv_heads", c_int), ("head_dim", c_int),
         ("page_size", c_int), ("num_pages", c_int), ("total_nodes", c_int), ("max_nodes", c_int),
         ("max_pages_per_seq", c_int), ("max_kv_pages", c_int), ("num_splits", c_int),
-        ("split_reduce", c_int), ("sm_scale", c_float),
+        ("split_reduce", c_int), ("sm_scale", c_float), ("flags", c_int),
         ("q", c_void_p), ("tree_k", c_void_p), ("tree_v", c_void_p), ("k_cache", c_void_p),
         ("v_cache", c_void_p), ("block_table", c_void_p), ("ctx_lens", c_void_p),
         ("cu_nodes", c_void_p), ("parents", c_void_p), ("kv_pages", c_void_p),
@@ -122,7 +123,7 @@ def sv_status_string(status: int) -> str:
 def make_attn_params(*, q, tree_k, tree_v, k_cache, v_cache, block_table, ctx_lens, cu_nodes, parents,
                      out, total_nodes: int, max_nodes: int, workspace=None, workspace_bytes: int = 0,
                      kv_pages=None, cu_kv_pages=None, max_kv_pages: int = 0, lse=None,
-                     sm_scale: float = 0.0, num_splits: int = 0, split_reduce: int = 0,
+                     sm_scale: float = 0.0, num_splits: int = 0, split_reduce: int = 0, flags: int = 0,
                      page_size: int = 16, batch=None,
                      num_q_heads=None, num_kv_heads=None, head_dim=None, num_pages=None,
                      max_pages_per_seq=None) -> sv_attn_params:
@@ -141,6 +142,7 @@ def make_attn_params(*, q, tree_k, tree_v, k_cache, v_cache, block_table, ctx_le
     p.num_splits = int(num_splits)
     p.split_reduce = int(split_reduce)
     p.sm_scale = float(sm_scale)
+    p.flags = int(flags)
     p.q, p.tree_k, p.tree_v = _ptr(q), _ptr(tree_k), _ptr(tree_v)
     p.k_cache, p.v_cache = _ptr(k_cache), _ptr(v_cache)
     p.block_table, p.ctx_lens, p.cu_nodes, p.parents = _ptr(block_table), _ptr(ctx_lens), _ptr(cu_nodes), _ptr(parents)

@@ -56,7 +56,7 @@ int device_sm_count() {
 
 extern "C" {
 
-int sv_abi_version(void) { return 1; }
+int sv_abi_version(void) { return 2; }
 
 const char* sv_status_string(sv_status status) {
   switch (status) {

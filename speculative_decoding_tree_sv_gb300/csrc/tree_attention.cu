@@ -8,28 +8,32 @@
 // keys followed by the tree keys, where the tree part of the mask keeps only
 // ancestors-or-self of i.
 //
-// Design (one CTA per (KV split, KV head x 256-row group, sequence)):
+// Design (one CTA per (KV split, KV head x 128-row tile, sequence)):
 //   * The M dimension of the contraction is (tree node x query head of the
-//     GQA group): rows r = node * G + g, two 128-row tiles per CTA.
+//     GQA group): rows r = node * G + g, one 128-row tile per CTA.
 //   * Context K/V pages (16 tokens, head-major inside a page) are gathered
-//     with TMA, eight pages (128 keys) per tile, 128-byte swizzled, into a
-//     ring of smem stages.  The tree's own K/V form one extra tile.
-//   * tcgen05.mma computes S = Q K^T (both operands K-major in smem) into
-//     TMEM; softmax warps read S with tcgen05.ld (one row per thread), apply
-//     the mask and an online, lazily rescaled softmax in base 2 (packed
-//     two-lane fp32 arithmetic), write P as bf16 back into the S columns, and
+//     with TMA, eight pages (128 keys) per tile, 128-byte swizzled, into
+//     rings of K and V stages.  The tree's own K/V form one extra tile.
+//   * The two row tiles of a (sequence, KV head) form a two-CTA cluster and
+//     read every K/V tile once: each CTA requests half of its pages with
+//     cluster multicast, so the tile lands in both CTAs' shared memory, and
+//     a stage is refilled only after both CTAs have released it.
+//   * Q lives in TMEM (the softmax warps load their rows and store them
+//     there), so shared memory holds only K and V stages: the loaded-DRAM
+//     latency times the bandwidth a CTA needs is what the rings must cover.
+//   * tcgen05.mma computes S = Q K^T (Q from TMEM, K K-major in smem) into
+//     one of two TMEM score buffers, so the tensor core computes the next
+//     tile's scores while the softmax warps work on the current ones.
+//     Softmax reads S with tcgen05.ld (one row per thread), applies the mask
+//     and an online, lazily rescaled base-2 softmax (packed two-lane fp32
+//     arithmetic), and writes P as bf16 back into the score columns;
 //     tcgen05.mma accumulates O += P V (P from TMEM, V MN-major in smem).
-//   * Warp roles: warp 0 loads (TMA), warp 1 issues MMAs (one thread),
-//     warps 4-7 and 8-11 run the softmax of row tiles 0 and 1.  The MMA
-//     issue order S0 S1 | PV0 S0' | PV1 S1' ... keeps the tensor core busy
-//     while the two softmax groups alternate.
-//   * KV splits are merged one of two ways.  Inside a cluster: the splits of
-//     one (sequence, head group) form a thread-block cluster, so they are
-//     co-resident; each writes its partial (O / l, log2-sum-exp) to the
-//     workspace, signals its peers' mbarriers, waits for theirs (bounded)
-//     and merges a slice of the rows from L2.  With a second kernel: for
-//     very long contexts, where more splits than fit in co-resident clusters
-//     pay off, the splits write partials that a combine kernel merges.
+//     TMEM columns: S0, S1, O, Q.  MMA order: S0 S1 | PV0 S2 | PV1 S3 | ...
+//   * Warp roles: warp 0 loads the K tiles, warp 3 the V tiles, warp 2
+//     resolves page ids ahead of them, warp 1 issues MMAs (one thread),
+//     warps 4-7 load Q, run the softmax and the epilogue.
+//   * KV splits write partials (O / l in bf16 and log2-sum-exp) to the
+//     workspace; a combine kernel merges them.
 //   * Launches allow programmatic dependent launch: the prologue (barriers,
 //     TMEM, descriptor prefetch) runs before the wait on the previous grid.
 #include <math.h>
@@ -41,42 +45,48 @@
 namespace sv {
 namespace attn {
 
-constexpr int kThreads = 384;
-// Registers per thread after the split: 128 x 56 (load + MMA group) + 256 x
-// 224 (softmax groups) = 64512 = 384 x 168, the launch allocation.
-constexpr int kRegsControl = 56;
-constexpr int kRegsSoftmax = 224;
-constexpr int kBlockN = 128;       // keys per tile (8 pages)
-constexpr int kTileRows = 128;     // rows per M tile
-constexpr int kCtaRows = 256;      // two M tiles per CTA
+constexpr int kThreads = 256;   // 4 control warps + one softmax warpgroup
+constexpr int kBlockN = 128;    // keys per tile (8 pages)
+constexpr int kTileRows = 128;  // rows per CTA (one M tile)
 constexpr int kPagesPerTile = kBlockN / 16;
-constexpr int kMaxClusterSplits = 16;
+// Page ids of the next tiles travel from the warp that resolves them to the
+// two loader warps through a small ring in shared memory.
+constexpr int kIdSlots = 8;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: defer O rescale until max grows by 2^8
 constexpr float kLn2 = 0.69314718055994530942f;
+constexpr uint16_t kPairMask = 0x3;  // both CTAs of a two-CTA cluster
 
-enum ReduceMode : int { kReduceNone = 0, kReduceCluster = 1, kReduceGlobal = 2 };
+enum ReduceMode : int { kReduceNone = 0, kReduceGlobal = 2 };
 
 template <int D>
 struct Cfg {
-  static constexpr int kHalves = D / 64;                   // 128-byte column halves
-  static constexpr int kStages = (D == 128) ? 2 : 4;
-  static constexpr uint32_t kHalfBytes = 128u * 128u;      // 128 rows x 128 B
-  static constexpr uint32_t kQTileBytes = kTileRows * D * 2;
-  static constexpr uint32_t kKVTileBytes = kBlockN * D * 2;
-  static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffK = kOffQ + 2 * kQTileBytes;
-  static constexpr uint32_t kOffV = kOffK + kStages * kKVTileBytes;
-  static constexpr uint32_t kOffBar = kOffV + kStages * kKVTileBytes;
-  static constexpr uint32_t kBarBytes = 512;
-  static constexpr uint32_t kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
+  static constexpr int kHalves = D / 64;                  // 128-byte column halves
+  // K stages return to the loader as soon as their QK^T is done, V stages
+  // only after PV: the V ring is the deeper one
+  static constexpr int kKStages = (D == 128) ? 3 : 5;
+  static constexpr int kVStages = (D == 128) ? 4 : 6;
+  static constexpr uint32_t kHalfBytes = 128u * 128u;     // 128 rows x 128 B
+  static constexpr uint32_t kTileBytes = kTileRows * D * 2;  // K and V tiles alike
+  static constexpr uint32_t kOffK = 0;
+  static constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
+  static constexpr uint32_t kOffBar = kOffV + kVStages * kTileBytes;
+  static constexpr uint32_t kBarBytes = 1024;
+  static constexpr uint32_t kOffIds = kOffBar + 512;      // int32 [kIdSlots][kPagesPerTile]
+  static constexpr uint32_t kOffParents = kOffBar + kBarBytes;  // int32 [kMaxNodes]
+  static constexpr uint32_t kSmemBytes = kOffParents + kMaxNodes * 4 + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColS0 = 0, kColS1 = 128;
-  static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
-  // epilogue staging of output rows (one padded row per softmax thread),
-  // over the Q/K/V stages once every MMA is done
-  static constexpr uint32_t kStageStride = D * 4 + 16;
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+  static constexpr uint32_t kColQ = kColO + D;  // Q as bf16 pairs: D / 2 columns
+  // epilogue staging of bf16 output rows (one padded row per softmax thread)
+  // over the K stages once every MMA and load is done
+  static constexpr uint32_t kStageStride = D * 2 + 16;
   static constexpr uint32_t kOffStage = 0;
-  static_assert(kOffStage + 2 * kTileRows * kStageStride <= kOffBar, "staging must fit below the barriers");
+  static_assert(kOffStage + kTileRows * kStageStride <= kOffBar, "staging must fit below the barriers");
+  static_assert((1 + 2 * kKStages + 2 * kVStages + 7 + 2 * kIdSlots) * 8 + 12 <= 512,
+                "barriers must fit below the id ring");
+  static_assert(512 + kIdSlots * kPagesPerTile * 4 <= kBarBytes - 8, "id ring must fit below the trace word");
+  static_assert(kColQ + D / 2 <= kTmemCols, "TMEM columns");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 struct Params {
@@ -86,6 +96,9 @@ struct Params {
   const int* parents;
   const int* kv_pages;
   const int* cu_kv_pages;
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k_cache;  // for L2 prefetch of whole (page, head) blocks
+  const __nv_bfloat16* v_cache;
   __nv_bfloat16* out;
   float* lse;
   __nv_bfloat16* part_o;  // split partials O / l (bf16), [splits][T * Hq][D]
@@ -94,34 +107,40 @@ struct Params {
   unsigned long long* trace;  // optional per-CTA phase timestamps
   long long trace_ctas;
   int num_q_heads;
+  int num_kv_heads;
   int group;  // G
   int num_pages;
   int max_pages_per_seq;
+  int max_nodes;
   int num_splits;
   int reduce_mode;
+  int early_ctx;  // read index arrays and context pages before the wait on the preceding grid
   int total_nodes;
-  int groups_per_seq;
+  int row_tiles;  // 128-row tiles per (sequence, KV head); even when paired
+  int paired;     // row tiles 2q, 2q+1 form a two-CTA cluster sharing K/V
   float scale_log2;
 };
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    tree_attention_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kc,
+    tree_attention_kernel(const __grid_constant__ CUtensorMap tm_kc,
                           const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_tk,
                           const __grid_constant__ CUtensorMap tm_tv, const __grid_constant__ Params p) {
   using C = Cfg<D>;
-  constexpr int NST = C::kStages;
+  constexpr int NSK = C::kKStages;
+  constexpr int NSV = C::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
   const int split = blockIdx.x;
-  const int kh = blockIdx.y / p.groups_per_seq;
-  const int mg = blockIdx.y % p.groups_per_seq;
+  const int kh = blockIdx.y / p.row_tiles;
+  const int rt = blockIdx.y % p.row_tiles;
   const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.group;
-  const bool cluster_mode = p.reduce_mode == kReduceCluster;
+  const bool paired = p.paired != 0;
+  const uint32_t rank = paired ? cluster_ctarank() : 0u;  // equals rt & 1 when paired
   // phase tracing (diagnostics): no live registers when it is off
   long long* trace_clk0 = reinterpret_cast<long long*>(smem + C::kOffBar + C::kBarBytes - 8);
   auto mark = [&](int ev) {
@@ -140,40 +159,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
-  uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;
-  uint64_t* v_full = k_full + NST;
-  uint64_t* k_empty = v_full + NST;
-  uint64_t* v_empty = k_empty + NST;
-  uint64_t* s_full = v_empty + NST;  // [2]
-  uint64_t* p_full = s_full + 2;     // [2]
-  uint64_t* o_final = p_full + 2;    // [2]
-  uint64_t* drain = o_final + 2;
-  uint64_t* published = drain + 1;   // cluster merge: every peer's partial is in the workspace
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(published + 1);
+  uint64_t* q_full = bars;          // Q rows stored in TMEM by the softmax warps
+  uint64_t* k_full = bars + 1;      // [NSK]
+  uint64_t* v_full = k_full + NSK;  // [NSV]
+  uint64_t* k_empty = v_full + NSV; // [NSK] released by this CTA's MMAs (and the peer's when paired)
+  uint64_t* v_empty = k_empty + NSK;  // [NSV]
+  uint64_t* s_full = v_empty + NSV;   // [2] scores of a buffer ready
+  uint64_t* p_full = s_full + 2;      // [2] probabilities of a buffer written
+  uint64_t* pv_done = p_full + 2;     // one phase per tile: O += P V finished
+  uint64_t* o_final = pv_done + 1;
+  uint64_t* drain = o_final + 1;
+  uint64_t* ids_full = drain + 1;             // [kIdSlots] page ids of a tile written
+  uint64_t* ids_empty = ids_full + kIdSlots;  // [kIdSlots] both loaders read them
+  int* ids = reinterpret_cast<int*>(smem + C::kOffIds);
+  int* par_s = reinterpret_cast<int*>(smem + C::kOffParents);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ids_empty + kIdSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* never_set = abort_flag + 1;  // drains wait on copies even after an abort
 
   // ---- prologue that reads no input: it may overlap the previous grid
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int i = 0; i < NST; ++i) {
+    mbar_init(q_full, kTileRows);
+    for (int i = 0; i < NSK; ++i) {
       mbar_init(k_full + i, 1);
+      mbar_init(k_empty + i, paired ? 2 : 1);
+    }
+    for (int i = 0; i < NSV; ++i) {
       mbar_init(v_full + i, 1);
-      mbar_init(k_empty + i, 1);
-      mbar_init(v_empty + i, 1);
+      mbar_init(v_empty + i, paired ? 2 : 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(s_full + t, 1);
       mbar_init(p_full + t, kTileRows);
-      mbar_init(o_final + t, 1);
     }
+    mbar_init(pv_done, 1);
+    mbar_init(o_final, 1);
     mbar_init(drain, 1);
-    mbar_init(published, p.num_splits);
+    for (int i = 0; i < kIdSlots; ++i) {
+      mbar_init(ids_full + i, 1);
+      mbar_init(ids_empty + i, 2);
+    }
     *abort_flag = 0;
     *never_set = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_kc);
     tma_prefetch_desc(&tm_vc);
     tma_prefetch_desc(&tm_tk);
@@ -186,23 +214,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // every CTA of a cluster reaches this point: peers' barriers are initialised
-  // before anyone can arrive on them remotely
-  if (cluster_mode) cluster_sync_all();
+  // both CTAs of a pair reach this point: the peer's barriers are initialised
+  // before any multicast copy or remote arrive can reach them
+  if (paired) cluster_sync_all();
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) mark(SV_TRACE_PROLOGUE);
-  griddep_wait();
+  // Everything below that reads what the preceding grid may write (Q, the
+  // tree's K/V) or writes what it may read (outputs, workspace) waits for it
+  // first; with early_ctx the index arrays and context pages are read
+  // before that wait.
+  if (!p.early_ctx) griddep_wait();
   griddep_launch_dependents();
   if (threadIdx.x == 0) mark(SV_TRACE_INPUTS);
 
   const int n0 = p.cu_nodes[b];
   const int N = p.cu_nodes[b + 1] - n0;
   const int L = p.ctx_lens[b];
+  if (threadIdx.x == 0 && split == 0 && rt == 0 && kh == 0 && (N < 1 || N > p.max_nodes))
+    report_error(p.err, SV_DEVERR_BAD_TREE);
   const int rows_total = N * G;
-  const int row0 = mg * kCtaRows;
-  // uniform over the cluster (its CTAs differ only in the split)
-  if (row0 < rows_total) {
-  const bool tile1 = row0 + kTileRows < rows_total;
+  const int row0 = rt * kTileRows;
+  // a pair works when either of its tiles has rows (uniform over the pair)
+  const int pair_row0 = paired ? (rt & ~1) * kTileRows : row0;
+  if (pair_row0 < rows_total) {
   const bool partial = p.kv_pages != nullptr;
   int n_pages, kvp0 = 0;
   if (partial) {
@@ -222,11 +256,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int jb = static_cast<int>(static_cast<long long>(split) * t_all / p.num_splits);
   const int je = static_cast<int>(static_cast<long long>(split + 1) * t_all / p.num_splits);
   const int ntiles = je - jb;
-  const bool work = ntiles > 0;
+  const bool work = ntiles > 0;  // uniform over the pair
 
   if (!work && p.reduce_mode == kReduceGlobal) {
     // empty split: publish an empty partial for our rows
-    if (threadIdx.x < kCtaRows) {
+    griddep_wait();
+    if (threadIdx.x < kTileRows) {
       const int row = row0 + threadIdx.x;
       if (row < rows_total) {
         const int node = row / G, g = row - (row / G) * G;
@@ -235,145 +270,197 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < 4) {
-    regs_decrease<kRegsControl>();
-    if (work && warp == 0) {
-      // ------------------------------------------------------------ producer
-      int k_issued = 0, v_issued = 0;
+    if (work && warp == 2) {
+      // ------------------------------------------------------------ page ids
+      // Resolves each context tile's eight page ids (partial list, then block
+      // table, both range-checked) into the id ring, up to kIdSlots tiles
+      // ahead of the loaders, and asks L2 for the K and V of the pages this
+      // CTA will request: the loads that follow then wait for L2, not DRAM,
+      // which keeps the stage rings short of their latency bound.
+      const int lane_lo = paired ? 4 * static_cast<int>(rank) : 0;
+      const int lane_hi = paired ? lane_lo + 4 : kPagesPerTile;
+      constexpr uint32_t kPageBytes = 16 * D * 2;
       bool ok = true;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(q_full, (tile1 ? 2u : 1u) * C::kQTileBytes);
-        for (int t = 0; t < (tile1 ? 2 : 1); ++t)
-          for (int h = 0; h < C::kHalves; ++h)
-            tma_load_3d(smem + C::kOffQ + t * C::kQTileBytes + h * C::kHalfBytes, &tm_q, q_full, h * 64, kh * G,
-                        n0 + (row0 + t * kTileRows) / G);
-      }
       for (int it = 0; it < ntiles; ++it) {
         const int j = jb + it;
-        const int st = it % NST;
-        const uint32_t ph = (it / NST) & 1;
-        const bool ctx = j < t_ctx;
-        int phys = 0;
-        if (ctx && lane < kPagesPerTile) {
+        const int sl = it % kIdSlots;
+        if (it >= kIdSlots) {
+          int w = (lane == 0) ? (mbar_wait(ids_empty + sl, ((it / kIdSlots) & 1) ^ 1u, abort_flag) ? 1 : 0) : 0;
+          if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+        }
+        if (j < t_ctx && lane < kPagesPerTile) {
           const int ps = min(j * kPagesPerTile + lane, n_pages - 1);  // ragged tail repeats the last page
           int lp = partial ? p.kv_pages[kvp0 + ps] : ps;
           if (lp < 0 || lp >= p.max_pages_per_seq) {
             report_error(p.err, SV_DEVERR_BAD_PAGE);
             lp = 0;
           }
-          phys = p.block_table[static_cast<size_t>(b) * p.max_pages_per_seq + lp];
+          int phys = p.block_table[static_cast<size_t>(b) * p.max_pages_per_seq + lp];
           if (phys < 0 || phys >= p.num_pages) {
             report_error(p.err, SV_DEVERR_BAD_PAGE);
             phys = 0;
           }
+          ids[sl * kPagesPerTile + lane] = phys;
+          if (lane >= lane_lo && lane < lane_hi) {
+            const size_t off = (static_cast<size_t>(phys) * p.num_kv_heads + kh) * (kPageBytes / 2);
+            l2_prefetch_bulk(p.k_cache + off, kPageBytes);
+            l2_prefetch_bulk(p.v_cache + off, kPageBytes);
+          }
         }
-        // K tile
-        if (it >= NST) {
-          int w = (lane == 0) ? (mbar_wait(k_empty + st, ph ^ 1u, abort_flag) ? 1 : 0) : 0;
-          if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
-        }
-        if (lane == 0) mbar_arrive_expect_tx(k_full + st, C::kKVTileBytes);
         __syncwarp();
-        uint8_t* kdst = smem + C::kOffK + st * C::kKVTileBytes;
-        if (ctx) {
-          if (lane < kPagesPerTile)
-            for (int h = 0; h < C::kHalves; ++h)
-              tma_load_4d(kdst + h * C::kHalfBytes + lane * 2048, &tm_kc, k_full + st, h * 64, 0, kh, phys);
-        } else if (lane == 0) {
-          for (int h = 0; h < C::kHalves; ++h) tma_load_3d(kdst + h * C::kHalfBytes, &tm_tk, k_full + st, h * 64, kh, n0);
+        if (lane == 0) {
+          if (it == 0) mark(SV_TRACE_FIRST_IDS);
+          mbar_arrive(ids_full + sl);
         }
-        k_issued = it + 1;
-        // V tile
-        if (it >= NST) {
-          int w = (lane == 0) ? (mbar_wait(v_empty + st, ph ^ 1u, abort_flag) ? 1 : 0) : 0;
-          if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
-        }
-        if (lane == 0) mbar_arrive_expect_tx(v_full + st, C::kKVTileBytes);
-        __syncwarp();
-        uint8_t* vdst = smem + C::kOffV + st * C::kKVTileBytes;
-        if (ctx) {
-          if (lane < kPagesPerTile)
-            for (int h = 0; h < C::kHalves; ++h)
-              tma_load_4d(vdst + h * C::kHalfBytes + lane * 2048, &tm_vc, v_full + st, h * 64, 0, kh, phys);
-        } else if (lane == 0) {
-          for (int h = 0; h < C::kHalves; ++h) tma_load_3d(vdst + h * C::kHalfBytes, &tm_tv, v_full + st, h * 64, kh, n0);
-        }
-        v_issued = it + 1;
       }
+      if (!ok && lane == 0) {
+        report_error(p.err, SV_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+    } else if (work && (warp == 0 || warp == 3)) {
+      // ------------------------------------------------------------ loaders
+      // warp 0 loads the K tiles, warp 3 the V tiles, each as far ahead as
+      // its ring allows.  When paired, each CTA requests four of a
+      // tile's eight pages (and one column half of the tree tile) with
+      // multicast to both CTAs; every CTA's full barrier expects the whole
+      // tile.
+      const bool is_k = warp == 0;
+      const CUtensorMap* tm_cache = is_k ? &tm_kc : &tm_vc;
+      const CUtensorMap* tm_tree = is_k ? &tm_tk : &tm_tv;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      uint8_t* ring = smem + (is_k ? C::kOffK : C::kOffV);
+      const int NS = is_k ? NSK : NSV;
+      const int lane_lo = paired ? 4 * static_cast<int>(rank) : 0;
+      const int lane_hi = paired ? lane_lo + 4 : kPagesPerTile;
+      int issued = 0;
+      // one tile into the ring; false when a bounded wait ran out
+      auto load_tile = [&](int it) -> bool {
+        const int j = jb + it;
+        const int st = it % NS;
+        const uint32_t ph = (it / NS) & 1;
+        const int sl = it % kIdSlots;
+        const bool ctx = j < t_ctx;
+        {
+          int w = (lane == 0) ? (mbar_wait(ids_full + sl, (it / kIdSlots) & 1, abort_flag) ? 1 : 0) : 0;
+          if (!__shfl_sync(0xffffffffu, w, 0)) return false;
+        }
+        const int phys = (ctx && lane < kPagesPerTile) ? ids[sl * kPagesPerTile + lane] : 0;
+        if (it >= NS) {
+          int w = (lane == 0) ? (mbar_wait(empty + st, ph ^ 1u, abort_flag) ? 1 : 0) : 0;
+          if (!__shfl_sync(0xffffffffu, w, 0)) return false;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(full + st, C::kTileBytes);
+        __syncwarp();
+        uint8_t* dst = ring + st * C::kTileBytes;
+        if (ctx) {
+          if (lane >= lane_lo && lane < lane_hi) {
+            for (int h = 0; h < C::kHalves; ++h) {
+              if (paired)
+                tma_load_4d_mc(dst + h * C::kHalfBytes + lane * 2048, tm_cache, full + st, h * 64, 0, kh, phys,
+                               kPairMask);
+              else
+                tma_load_4d(dst + h * C::kHalfBytes + lane * 2048, tm_cache, full + st, h * 64, 0, kh, phys);
+            }
+          }
+        } else if (lane == 0) {
+          for (int h = 0; h < C::kHalves; ++h) {
+            if (!paired)
+              tma_load_3d(dst + h * C::kHalfBytes, tm_tree, full + st, h * 64, kh, n0);
+            else if (C::kHalves == 2 ? h == static_cast<int>(rank) : rank == 0u)
+              tma_load_3d_mc(dst + h * C::kHalfBytes, tm_tree, full + st, h * 64, kh, n0, kPairMask);
+          }
+        }
+        issued = it + 1;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ids_empty + sl);
+        return true;
+      };
+      bool ok = true;
+      int it = 0;
+      if (p.early_ctx) {
+        // Context pages are not written by the preceding grid: the first
+        // ring's worth of them is requested before waiting for it.
+        for (; ok && it < ntiles && it < NS && jb + it < t_ctx; ++it) ok = load_tile(it);
+      }
+      griddep_wait();  // the tree's K/V come from the preceding grid
+      for (; ok && it < ntiles; ++it) ok = load_tile(it);
       if (!ok && lane == 0) {
         // Timed out: stop the other roles, then let our copies land before exit.
         report_error(p.err, SV_DEVERR_TIMEOUT);
         *abort_flag = 1;
-        mbar_wait(q_full, 0, never_set);
-        for (int it = max(0, k_issued - NST); it < k_issued; ++it)
-          mbar_wait(k_full + (it % NST), (it / NST) & 1, never_set);
-        for (int it = max(0, v_issued - NST); it < v_issued; ++it)
-          mbar_wait(v_full + (it % NST), (it / NST) & 1, never_set);
+        for (int i = max(0, issued - NS); i < issued; ++i) mbar_wait(full + (i % NS), (i / NS) & 1, never_set);
       }
     } else if (work && warp == 1) {
       // ------------------------------------------------------------ MMA issuer
       if (lane == 0) {
         constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kBlockN, false, false);
         constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
-        const int nt = tile1 ? 2 : 1;
-        const uint32_t q_base = smem_u32(smem + C::kOffQ);
         const uint32_t k_base = smem_u32(smem + C::kOffK);
         const uint32_t v_base = smem_u32(smem + C::kOffV);
-        bool ok = mbar_wait(q_full, 0, abort_flag);
-        auto issue_qk = [&](int t, int st) {
-          const uint32_t d = tmem + (t ? C::kColS1 : C::kColS0);
-  #pragma unroll
+        // S = Q K^T: Q (bf16 pairs) from TMEM, K K-major from shared memory
+        auto issue_qk = [&](int buf, int kst) {
+          const uint32_t d = tmem + (buf ? C::kColS1 : C::kColS0);
+#pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-            const uint64_t a = smem_desc_sw128(q_base + t * C::kQTileBytes + off, 16, 1024);
-            const uint64_t bdesc = smem_desc_sw128(k_base + st * C::kKVTileBytes + off, 16, 1024);
-            umma_ss(d, a, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+            const uint64_t bdesc = smem_desc_sw128(k_base + kst * C::kTileBytes + off, 16, 1024);
+            umma_ts(d, tmem + C::kColQ + kk * 8, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
           }
         };
-        auto issue_pv = [&](int t, int st, bool accumulate) {
-          const uint32_t d = tmem + (t ? C::kColO1 : C::kColO0);
-          const uint32_t a = tmem + (t ? C::kColS1 : C::kColS0);
-  #pragma unroll
+        // O += P V: P (bf16 pairs) in the score buffer's first columns
+        auto issue_pv = [&](int buf, int vst, bool accumulate) {
+          const uint32_t d = tmem + C::kColO;
+          const uint32_t a = tmem + (buf ? C::kColS1 : C::kColS0);
+#pragma unroll
           for (int kk = 0; kk < kBlockN / 16; ++kk) {
-            const uint64_t bdesc = smem_desc_sw128(v_base + st * C::kKVTileBytes + kk * 2048, C::kHalfBytes, 1024);
+            const uint64_t bdesc = smem_desc_sw128(v_base + vst * C::kTileBytes + kk * 2048, C::kHalfBytes, 1024);
             umma_ts(d, a + kk * 8, bdesc, idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
           }
         };
-        if (ok) ok = mbar_wait(k_full, 0, abort_flag);
-        if (ok) {
-          tc_fence_after();
-          mark(SV_TRACE_FIRST_MMA);
-          for (int t = 0; t < nt; ++t) {
-            issue_qk(t, 0);
-            umma_commit(s_full + t);
+        // A stage goes back to the loaders of both CTAs of a pair once this
+        // CTA's MMAs have read it.  The last stages of a ring are never
+        // refilled, so they are not released: no arrive is left in flight
+        // towards the peer when the CTAs finish.
+        auto release = [&](uint64_t* bar, int it, int ns) {
+          if (it + ns < ntiles) {
+            if (paired) umma_commit_mc(bar, kPairMask);
+            else umma_commit(bar);
           }
-          umma_commit(k_empty);
+        };
+        bool ok = mbar_wait(q_full, 0, abort_flag);
+        // scores of the first two tiles, one per buffer
+        for (int it = 0; ok && it < 2 && it < ntiles; ++it) {
+          if (!mbar_wait(k_full + it % NSK, (it / NSK) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          if (it == 0) mark(SV_TRACE_FIRST_MMA);
+          issue_qk(it, it % NSK);
+          umma_commit(s_full + it);
+          release(k_empty + it % NSK, it, NSK);
         }
         for (int it = 0; ok && it < ntiles; ++it) {
-          const int st = it % NST;
-          const uint32_t ph = (it / NST) & 1;
-          const int nx = it + 1;
-          const int st2 = nx % NST;
-          const uint32_t ph2 = (nx / NST) & 1;
-          if (!mbar_wait(v_full + st, ph, abort_flag)) { ok = false; break; }
-          for (int t = 0; t < nt; ++t) {
-            if (!mbar_wait(p_full + t, it & 1, abort_flag)) { ok = false; break; }
+          const int buf = it & 1;
+          const int vst = it % NSV;
+          if (!mbar_wait(v_full + vst, (it / NSV) & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(p_full + buf, (it >> 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(buf, vst, it > 0);
+          umma_commit(pv_done);
+          release(v_empty + vst, it, NSV);
+          // the next scores of this buffer overwrite P(it) after PV(it) has
+          // read it: tcgen05 MMAs of one thread execute in issue order
+          const int nx = it + 2;
+          if (nx < ntiles) {
+            const int kst = nx % NSK;
+            if (!mbar_wait(k_full + kst, (nx / NSK) & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            issue_pv(t, st, it > 0);
-            if (nx < ntiles) {
-              if (t == 0) {
-                if (!mbar_wait(k_full + st2, ph2, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-              }
-              issue_qk(t, st2);
-              umma_commit(s_full + t);
-            }
+            issue_qk(buf, kst);
+            umma_commit(s_full + buf);
+            release(k_empty + kst, nx, NSK);
           }
-          if (!ok) break;
-          umma_commit(v_empty + st);
-          if (nx < ntiles) umma_commit(k_empty + st2);
         }
         if (ok) {
-          for (int t = 0; t < nt; ++t) umma_commit(o_final + t);
+          umma_commit(o_final);
         } else {
           report_error(p.err, SV_DEVERR_TIMEOUT);
           *abort_flag = 1;
@@ -384,37 +471,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     }
   } else {
-    regs_increase<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
-    const int t = (warp - 4) >> 2;
-    const int qw = warp & 3;
-    const int r = qw * 32 + lane;
-    const int r_cta = t * kTileRows + r;
-    const int row = row0 + r_cta;
+    const int qw = warp - 4;
+    const int r = qw * 32 + lane;  // TMEM lane = row of the tile
+    const int row = row0 + r;
     const bool row_exists = row < rows_total;
-    const bool active = work && (t == 0 || tile1);  // warp-uniform
     const int node = row / G;
     const int g = row - node * G;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(qw * 32) << 16);
-    const uint32_t col_s = t ? C::kColS1 : C::kColS0;
-    const uint32_t col_o = t ? C::kColO1 : C::kColO0;
+    const size_t orow = static_cast<size_t>(n0 + node) * p.num_q_heads + kh * G + g;
     float m_run = -INFINITY;
     float l_run = 0.f;
     bool ok = true;
-    if (active) {
-        // ancestor-or-self bitmask of this row's node (only the split that
-        // owns the tree tile needs it)
-        uint32_t anc0 = 0, anc1 = 0, anc2 = 0, anc3 = 0;
-        if (je == t_all && row_exists) {
+    if (work) {
+      // Q: each thread moves its row (zeros past the tree) into TMEM as bf16
+      // pairs, the A operand of QK^T
+      griddep_wait();  // Q comes from the preceding grid
+      {
+        const uint4* src = reinterpret_cast<const uint4*>(p.q + orow * D);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t qv[32];
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const uint4 t = row_exists ? __ldg(src + c * 8 + v) : make_uint4(0u, 0u, 0u, 0u);
+            qv[4 * v + 0] = t.x;
+            qv[4 * v + 1] = t.y;
+            qv[4 * v + 2] = t.z;
+            qv[4 * v + 3] = t.w;
+          }
+          tmem_st32(lane_base + C::kColQ + c * 32, qv);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(q_full);
+      }
+      // ancestor-or-self bitmask of this row's node (only the split that
+      // owns the tree tile needs it): the tree's parents are staged in shared
+      // memory with one coalesced load, then each row walks its chain there
+      uint32_t anc0 = 0, anc1 = 0, anc2 = 0, anc3 = 0;
+      if (je == t_all) {
+        for (int i = r; i < N && i < kMaxNodes; i += kTileRows) par_s[i] = p.parents[n0 + i];
+        named_barrier(1, kTileRows);
+        if (row_exists) {
           int c = node;
-          for (int step = 0; step < kMaxNodes && c >= 0 && c < kMaxNodes; ++step) {
+          for (int step = 0; step < kMaxNodes && c >= 0 && c < kMaxNodes && c < N; ++step) {
             const uint32_t bit = 1u << (c & 31);
             if ((c >> 5) == 0) anc0 |= bit;
             else if ((c >> 5) == 1) anc1 |= bit;
             else if ((c >> 5) == 2) anc2 |= bit;
             else anc3 |= bit;
             if (c == 0) break;
-            const int pc = p.parents[n0 + c];
+            const int pc = par_s[c];
             if (pc < 0 || pc >= c) {
               report_error(p.err, SV_DEVERR_BAD_PARENT);
               break;
@@ -422,102 +530,102 @@ __global__ void __launch_bounds__(kThreads, 1)
             c = pc;
           }
         }
-
-        if (t == 0 && r == 0 && je == t_all) mark(SV_TRACE_TREE_MASK);
-        for (int it = 0; it < ntiles; ++it) {
-          const int j = jb + it;
-          // warp-uniform outcome: the TMEM loads below are warp-collective
-          if (!__all_sync(0xffffffffu, mbar_wait(s_full + t, it & 1, abort_flag))) { ok = false; break; }
-          tc_fence_after();
-          if (it == 0 && t == 0 && r == 0) mark(SV_TRACE_FIRST_S);
-          uint32_t sr[kBlockN];
-  #pragma unroll
-          for (int c = 0; c < kBlockN / 32; ++c)
-            tmem_ld32(lane_base + col_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
-          tmem_ld_wait();
-          // mask: only the ragged last context tile and the tree tile need one
-          constexpr uint32_t kNegInf = 0xFF800000u;
-          if (j >= t_ctx) {
-  #pragma unroll
-            for (int k = 0; k < kBlockN; ++k) {
-              const uint32_t w = (k < 32) ? anc0 : (k < 64) ? anc1 : (k < 96) ? anc2 : anc3;
-              if (!((k < N) && ((w >> (k & 31)) & 1u))) sr[k] = kNegInf;
-            }
-          } else if (j == t_ctx - 1) {
-            const int nvalid = (n_pages - kPagesPerTile * j - 1) * 16 + last_page_tokens;
-  #pragma unroll
-            for (int k = 0; k < kBlockN; ++k)
-              if (k >= nvalid) sr[k] = kNegInf;
+        if (r == 0) mark(SV_TRACE_TREE_MASK);
+      }
+      for (int it = 0; it < ntiles; ++it) {
+        const int j = jb + it;
+        const int buf = it & 1;
+        const uint32_t col_s = buf ? C::kColS1 : C::kColS0;
+        // warp-uniform outcome: the TMEM loads below are warp-collective
+        if (!__all_sync(0xffffffffu, mbar_wait(s_full + buf, (it >> 1) & 1, abort_flag))) { ok = false; break; }
+        tc_fence_after();
+        if (it == 0 && r == 0) mark(SV_TRACE_FIRST_S);
+        uint32_t sr[kBlockN];
+#pragma unroll
+        for (int c = 0; c < kBlockN / 32; ++c)
+          tmem_ld32(lane_base + col_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + c * 32));
+        tmem_ld_wait();
+        // mask: only the ragged last context tile and the tree tile need one
+        constexpr uint32_t kNegInf = 0xFF800000u;
+        if (j >= t_ctx) {
+#pragma unroll
+          for (int k = 0; k < kBlockN; ++k) {
+            const uint32_t w = (k < 32) ? anc0 : (k < 64) ? anc1 : (k < 96) ? anc2 : anc3;
+            if (!((k < N) && ((w >> (k & 31)) & 1u))) sr[k] = kNegInf;
           }
-          // row maximum of the raw scores (scale > 0 commutes with max)
-          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-  #pragma unroll
-          for (int k = 0; k < kBlockN; k += 8) {
-            mx0 = max3(mx0, __uint_as_float(sr[k + 0]), __uint_as_float(sr[k + 1]));
-            mx1 = max3(mx1, __uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3]));
-            mx2 = max3(mx2, __uint_as_float(sr[k + 4]), __uint_as_float(sr[k + 5]));
-            mx3 = max3(mx3, __uint_as_float(sr[k + 6]), __uint_as_float(sr[k + 7]));
-          }
-          const float tmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
-          const float m_new = fmaxf(m_run, tmax);
-          const bool grow = m_new > m_run + kRescaleThreshold;
-          // The O rescale reads and writes TMEM with warp-collective
-          // instructions: the whole warp takes it when any row needs it
-          // (rows that do not are scaled by 1).
-          if (it > 0 && __any_sync(0xffffffffu, grow)) {
-            // O already holds earlier tiles (their PV finished before this S
-            // was committed): rescale it and the running sum.
-            {
-              const float f = grow ? ex2(m_run - m_new) : 1.f;
-              l_run *= f;
-              const uint64_t f2 = f2_pack(f, f);
-              uint32_t o[32];
-  #pragma unroll
-              for (int c = 0; c < D / 32; ++c) {
-                tmem_ld32(lane_base + col_o + c * 32, o);
-                tmem_ld_wait();
-  #pragma unroll
-                for (int k = 0; k < 32; k += 2) {
-                  const uint64_t v = f2_mul(f2_pack(__uint_as_float(o[k]), __uint_as_float(o[k + 1])), f2);
-                  o[k] = static_cast<uint32_t>(v);
-                  o[k + 1] = static_cast<uint32_t>(v >> 32);
-                }
-                tmem_st32(lane_base + col_o + c * 32, o);
-              }
-              tmem_st_wait();
-            }
-          }
-          if (grow) m_run = m_new;
-          const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-          // p = 2^(s * scale_log2 - m), packed two at a time
-          const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
-          const uint64_t nm2 = f2_pack(-m_use, -m_use);
-          uint64_t acc0 = 0, acc1 = 0;
-          uint32_t pk[kBlockN / 2];
-  #pragma unroll
-          for (int k = 0; k < kBlockN; k += 4) {
-            const uint64_t a = f2_fma(f2_pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), sc2, nm2);
-            const uint64_t b = f2_fma(f2_pack(__uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3])), sc2, nm2);
-            const float p0 = ex2(f2_lo(a)), p1 = ex2(f2_hi(a));
-            const float p2 = ex2(f2_lo(b)), p3 = ex2(f2_hi(b));
-            acc0 = f2_add(acc0, f2_pack(p0, p1));
-            acc1 = f2_add(acc1, f2_pack(p2, p3));
-            pk[k >> 1] = pack_bf16x2(p0, p1);
-            pk[(k >> 1) + 1] = pack_bf16x2(p2, p3);
-          }
-          const uint64_t acc = f2_add(acc0, acc1);
-          l_run += f2_lo(acc) + f2_hi(acc);
-  #pragma unroll
-          for (int c = 0; c < kBlockN / 64; ++c)
-            tmem_st32(lane_base + col_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(pk + c * 32));
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(p_full + t);
+        } else if (j == t_ctx - 1) {
+          const int nvalid = (n_pages - kPagesPerTile * j - 1) * 16 + last_page_tokens;
+#pragma unroll
+          for (int k = 0; k < kBlockN; ++k)
+            if (k >= nvalid) sr[k] = kNegInf;
         }
-        if (t == 0 && r == 0) mark(SV_TRACE_LOOP_END);
-
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_final + t, 0, abort_flag));
-      if (t == 0 && r == 0) mark(SV_TRACE_O_READY);
+        // row maximum of the raw scores (scale > 0 commutes with max)
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kBlockN; k += 8) {
+          mx0 = max3(mx0, __uint_as_float(sr[k + 0]), __uint_as_float(sr[k + 1]));
+          mx1 = max3(mx1, __uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3]));
+          mx2 = max3(mx2, __uint_as_float(sr[k + 4]), __uint_as_float(sr[k + 5]));
+          mx3 = max3(mx3, __uint_as_float(sr[k + 6]), __uint_as_float(sr[k + 7]));
+        }
+        const float tmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * p.scale_log2;
+        const float m_new = fmaxf(m_run, tmax);
+        const bool grow = m_new > m_run + kRescaleThreshold;
+        // The O rescale reads and writes TMEM with warp-collective
+        // instructions: the whole warp takes it when any row needs it (rows
+        // that do not are scaled by 1).  O holds tiles up to it - 1; the PV
+        // of tile it - 1 may still be running, so wait for it first.
+        if (it > 0 && __any_sync(0xffffffffu, grow)) {
+          if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (it - 1) & 1, abort_flag))) { ok = false; break; }
+          tc_fence_after();
+          const float f = grow ? ex2(m_run - m_new) : 1.f;
+          l_run *= f;
+          const uint64_t f2 = f2_pack(f, f);
+          uint32_t o[32];
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            tmem_ld32(lane_base + C::kColO + c * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+              const uint64_t v = f2_mul(f2_pack(__uint_as_float(o[k]), __uint_as_float(o[k + 1])), f2);
+              o[k] = static_cast<uint32_t>(v);
+              o[k + 1] = static_cast<uint32_t>(v >> 32);
+            }
+            tmem_st32(lane_base + C::kColO + c * 32, o);
+          }
+          tmem_st_wait();
+        }
+        if (grow) m_run = m_new;
+        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        // p = 2^(s * scale_log2 - m), packed two at a time
+        const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2);
+        const uint64_t nm2 = f2_pack(-m_use, -m_use);
+        uint64_t acc0 = 0, acc1 = 0;
+        uint32_t pk[kBlockN / 2];
+#pragma unroll
+        for (int k = 0; k < kBlockN; k += 4) {
+          const uint64_t a = f2_fma(f2_pack(__uint_as_float(sr[k]), __uint_as_float(sr[k + 1])), sc2, nm2);
+          const uint64_t bb = f2_fma(f2_pack(__uint_as_float(sr[k + 2]), __uint_as_float(sr[k + 3])), sc2, nm2);
+          const float p0 = ex2(f2_lo(a)), p1 = ex2(f2_hi(a));
+          const float p2 = ex2(f2_lo(bb)), p3 = ex2(f2_hi(bb));
+          acc0 = f2_add(acc0, f2_pack(p0, p1));
+          acc1 = f2_add(acc1, f2_pack(p2, p3));
+          pk[k >> 1] = pack_bf16x2(p0, p1);
+          pk[(k >> 1) + 1] = pack_bf16x2(p2, p3);
+        }
+        const uint64_t acc = f2_add(acc0, acc1);
+        l_run += f2_lo(acc) + f2_hi(acc);
+#pragma unroll
+        for (int c = 0; c < kBlockN / 64; ++c)
+          tmem_st32(lane_base + col_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(pk + c * 32));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full + buf);
+      }
+      if (r == 0) mark(SV_TRACE_LOOP_END);
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_final, 0, abort_flag));
+      if (r == 0) mark(SV_TRACE_O_READY);
       if (!ok && lane == 0) {
         report_error(p.err, SV_DEVERR_TIMEOUT);
         *abort_flag = 1;
@@ -525,38 +633,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------------------------------------------------- epilogue
-    const bool have_o = active && ok;  // warp-uniform
+    griddep_wait();  // outputs and workspace may still be in use by the preceding grid
+    const bool have_o = work && ok;  // warp-uniform
     if (have_o) tc_fence_after();
     const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
     const float lse2 = (have_o && l_run > 0.f) ? m_run + log2f(l_run) : -INFINITY;
-    const size_t orow = static_cast<size_t>(n0 + node) * p.num_q_heads + kh * G + g;
     // Output rows leave through shared memory: each thread parks its row
-    // (one TMEM lane) in a padded staging row over the dead Q/K/V stages
-    // (every MMA finished before o_final fired), then the warp writes whole
-    // rows, lane l moving chunk l, so global stores are coalesced.
+    // (one TMEM lane) in a padded staging row over the dead K stages (every
+    // MMA and every load has finished once o_final fired), then the warp
+    // writes whole rows, lane l moving chunk l, so global stores are
+    // coalesced.
     const bool partial_out = p.reduce_mode != kReduceNone;
     if (have_o) {
-      uint32_t o[D];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32(lane_base + col_o + c * 32, *reinterpret_cast<uint32_t(*)[32]>(o + c * 32));
-      tmem_ld_wait();
-      uint8_t* stage = smem + C::kOffStage + (warp - 4) * 32 * C::kStageStride;
+      uint8_t* stage = smem + C::kOffStage + qw * 32 * C::kStageStride;
       uint8_t* mine = stage + lane * C::kStageStride;
 #pragma unroll
-      for (int v = 0; v < D / 8; ++v) {
-        uint4 w;
-        w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
-        w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
-        w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
-        w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
-        reinterpret_cast<uint4*>(mine)[v] = w;
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + C::kColO + c * 32, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
+          w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
+          w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
+          w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
+          reinterpret_cast<uint4*>(mine + c * 64)[v] = w;
+        }
       }
       __syncwarp();
       // rows of D bf16 = D / 8 16-byte chunks; the warp stores 256 / D rows per
       // instruction
       constexpr int kChunks = D / 8;
       constexpr int kRowsPerPass = 32 / kChunks;
-      const int wrow0 = row0 + t * kTileRows + qw * 32;
+      const int wrow0 = row0 + qw * 32;
       const int nrows = min(32, rows_total - wrow0);
       const size_t split_base = partial_out ? static_cast<size_t>(split) * p.total_nodes * p.num_q_heads : 0;
       const long long my_out_row = static_cast<long long>(split_base + orow);  // this lane's row
@@ -571,110 +682,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (p.reduce_mode == kReduceNone) {
       if (have_o && row_exists && p.lse != nullptr) p.lse[orow] = lse2 * kLn2;
-      if (r_cta == 0) mark(SV_TRACE_EPILOGUE);
-    } else if (p.reduce_mode == kReduceGlobal) {
-      if (row_exists && (t == 0 || tile1))
-        p.part_lse[static_cast<size_t>(split) * p.total_nodes * p.num_q_heads + orow] = lse2;
-    } else {
-      // ---- merge inside the cluster (one CTA per split, co-resident)
-      // Each CTA has written its partial rows (O / l and log2-sum-exp, fp32)
-      // to the workspace; it tells its peers through their mbarriers
-      // (release at cluster scope), waits until every peer has done the same
-      // (bounded), then merges its own slice of the rows from the peers'
-      // partials, which sit in L2.  Global memory outlives the CTAs: no exit
-      // handshake is needed.
-      const int S = p.num_splits;
-      const int rank = static_cast<int>(cluster_ctarank());
-      const size_t split_stride = static_cast<size_t>(p.total_nodes) * p.num_q_heads;
-      if (row_exists && (t == 0 || tile1)) p.part_lse[static_cast<size_t>(split) * split_stride + orow] = lse2;
-      if (r_cta == 0) mark(SV_TRACE_EPILOGUE);
-      named_barrier(1, 2 * kTileRows);
-      if (threadIdx.x == 4 * 32) {
-        for (int rk = 0; rk < S; ++rk) mbar_arrive_cluster(mapa_shared(smem_u32(published), rk));
-      }
-      if (mbar_wait_cluster(published, 0)) {
-        if (r_cta == 0) mark(SV_TRACE_MERGE_READY);
-        constexpr int E = D / 32;  // output elements per lane
-        constexpr int R = 2;       // rows merged together (their loads overlap)
-        const int rows_cta = min(kCtaRows, rows_total - row0);
-        const int slice = (rows_cta + S - 1) / S;
-        const int lo = rank * slice, hi = min(rows_cta, lo + slice);
-        for (int rb = lo + (warp - 4) * R; rb < hi; rb += 8 * R) {
-          size_t out_row[R];
-          float ls[R];
-          float4 v4[R][kMaxClusterSplits];
-#pragma unroll
-          for (int q = 0; q < R; ++q) {
-            const int rr = min(rb + q, hi - 1);  // a duplicate row is merged twice, harmlessly
-            const int grow = row0 + rr;
-            const int gnode = grow / G;
-            out_row[q] = static_cast<size_t>(n0 + gnode) * p.num_q_heads + kh * G + (grow - gnode * G);
-            ls[q] = (lane < S) ? __ldcg(p.part_lse + lane * split_stride + out_row[q]) : -INFINITY;
-#pragma unroll
-            for (int s = 0; s < kMaxClusterSplits; ++s) {
-              if (s < S) {
-                const __nv_bfloat16* src = p.part_o + (s * split_stride + out_row[q]) * D + lane * E;
-                if constexpr (E == 4) {
-                  const uint2 v = __ldcg(reinterpret_cast<const uint2*>(src));
-                  v4[q][s] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u),
-                                         __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
-                } else {
-                  const uint32_t v = __ldcg(reinterpret_cast<const unsigned int*>(src));
-                  v4[q][s] = make_float4(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u), 0.f, 0.f);
-                }
-              }
-            }
-          }
-#pragma unroll
-          for (int q = 0; q < R; ++q) {
-            if (rb + q >= hi) break;
-            float mx = ls[q];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            const float w = (ls[q] == -INFINITY) ? 0.f : ex2(ls[q] - mx);
-            float wsum = w;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-            float acc[E];
-#pragma unroll
-            for (int e = 0; e < E; ++e) acc[e] = 0.f;
-#pragma unroll
-            for (int s = 0; s < kMaxClusterSplits; ++s) {
-              if (s < S) {
-                const float ws = __shfl_sync(0xffffffffu, w, s);
-                if (ws != 0.f) {  // skipped peers may hold stale, non-finite rows
-                  acc[0] += ws * v4[q][s].x;
-                  acc[1] += ws * v4[q][s].y;
-                  if constexpr (E == 4) {
-                    acc[2] += ws * v4[q][s].z;
-                    acc[3] += ws * v4[q][s].w;
-                  }
-                }
-              }
-            }
-            const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
-            __nv_bfloat16* dst = p.out + out_row[q] * D + lane * E;
-            if constexpr (E == 4) {
-              uint2 v;
-              v.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-              v.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-              *reinterpret_cast<uint2*>(dst) = v;
-            } else {
-              *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-            }
-            if (lane == 0 && p.lse != nullptr) p.lse[out_row[q]] = (mx + log2f(wsum)) * kLn2;
-          }
-        }
-      } else if (lane == 0) {
-        report_error(p.err, SV_DEVERR_TIMEOUT);
-      }
-      if (r_cta == 0) mark(SV_TRACE_MERGE_DONE);
+    } else if (row_exists) {
+      p.part_lse[static_cast<size_t>(split) * p.total_nodes * p.num_q_heads + orow] = lse2;
     }
+    if (r == 0) mark(SV_TRACE_EPILOGUE);
   }
-  }  // row group exists
+  }  // the pair has rows
 
   tc_fence_before();
   __syncthreads();
+  // neither CTA of a pair leaves while the other may still address its
+  // shared memory (multicast copies, remote arrives); every path of both CTAs
+  // reaches this point, since every other wait is bounded
+  if (paired) cluster_sync_all();
   if (threadIdx.x == 0) mark(SV_TRACE_EXIT);
   if (warp == 1) {
     tc_fence_after();
@@ -683,40 +703,65 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Merge split partials: O = sum_s w_s O_s / sum_s w_s, w_s = 2^(lse_s - max).
+// One warp per output row: lane s holds split s's (and s + 32's) log2-sum-exp,
+// the weights come from warp reductions, and the partial rows are read eight
+// splits at a time so their loads overlap.  It lets the next grid in the
+// stream launch early (programmatic dependent launch): a following attention
+// grid then runs its prologue while this one merges.
 template <int D>
 __global__ void __launch_bounds__(256) split_combine_kernel(const __nv_bfloat16* __restrict__ part_o,
                                                             const float* __restrict__ part_lse,
                                                             __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
                                                             int rows, int splits) {
   constexpr int E = D / 32;  // elements per lane
+  griddep_launch_dependents();
+  griddep_wait();
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
-  float mx = -INFINITY;
-  for (int s = 0; s < splits; ++s) mx = fmaxf(mx, part_lse[static_cast<size_t>(s) * rows + row]);
+  const float l0 = (lane < splits) ? __ldcg(part_lse + static_cast<size_t>(lane) * rows + row) : -INFINITY;
+  const float l1 = (lane + 32 < splits) ? __ldcg(part_lse + static_cast<size_t>(lane + 32) * rows + row) : -INFINITY;
+  float mx = fmaxf(l0, l1);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float w0 = (l0 == -INFINITY) ? 0.f : ex2(l0 - mx);
+  const float w1 = (l1 == -INFINITY) ? 0.f : ex2(l1 - mx);
+  float wsum = w0 + w1;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
-  for (int s = 0; s < splits; ++s) {
-    const float ls = part_lse[static_cast<size_t>(s) * rows + row];
-    if (ls == -INFINITY) continue;
-    const float w = ex2(ls - mx);
-    wsum += w;
-    const __nv_bfloat16* src = part_o + (static_cast<size_t>(s) * rows + row) * D + lane * E;
-    if constexpr (E == 4) {
-      const uint2 v = *reinterpret_cast<const uint2*>(src);
-      acc[0] += w * __uint_as_float(v.x << 16);
-      acc[1] += w * __uint_as_float(v.x & 0xFFFF0000u);
-      acc[2] += w * __uint_as_float(v.y << 16);
-      acc[3] += w * __uint_as_float(v.y & 0xFFFF0000u);
-    } else {
-      const uint32_t v = *reinterpret_cast<const uint32_t*>(src);
-      acc[0] += w * __uint_as_float(v << 16);
-      acc[1] += w * __uint_as_float(v & 0xFFFF0000u);
+  for (int s0 = 0; s0 < splits; s0 += 8) {
+    float ws[8];
+    uint32_t v[8][E / 2];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int s = s0 + k;
+      ws[k] = __shfl_sync(0xffffffffu, (s < 32) ? w0 : w1, s & 31);
+#pragma unroll
+      for (int e = 0; e < E / 2; ++e) v[k][e] = 0u;
+      // empty splits (weight 0) may hold stale rows: never read them
+      if (s < splits && ws[k] != 0.f) {
+        const __nv_bfloat16* src = part_o + (static_cast<size_t>(s) * rows + row) * D + lane * E;
+        if constexpr (E == 4) {
+          const uint2 t = __ldcg(reinterpret_cast<const uint2*>(src));
+          v[k][0] = t.x;
+          v[k][1] = t.y;
+        } else {
+          v[k][0] = __ldcg(reinterpret_cast<const unsigned int*>(src));
+        }
+      }
     }
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+#pragma unroll
+      for (int e = 0; e < E / 2; ++e) {
+        acc[2 * e] += ws[k] * __uint_as_float(v[k][e] << 16);
+        acc[2 * e + 1] += ws[k] * __uint_as_float(v[k][e] & 0xFFFF0000u);
+      }
   }
-  const float inv = 1.f / wsum;
+  const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
   __nv_bfloat16* dst = out + static_cast<size_t>(row) * D + lane * E;
   if constexpr (E == 4) {
     uint2 w;
@@ -737,7 +782,8 @@ long long g_trace_ctas = 0;
 
 struct Plan {
   int group;
-  int groups_per_seq;
+  int row_tiles;
+  int paired;
   int splits;
   int mode;
   size_t workspace;
@@ -747,7 +793,8 @@ sv_status validate(const sv_attn_params* p) {
   if (p == nullptr) return SV_ERR_INVALID_ARG;
   if (p->batch < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1 || p->total_nodes < 0 || p->max_nodes < 1 ||
       p->max_pages_per_seq < 1 || p->num_pages < 1 || p->num_splits < 0 || p->max_kv_pages < 0 ||
-      p->split_reduce < 0 || p->split_reduce > 2)
+      (p->split_reduce != 0 && p->split_reduce != 2) ||
+      (p->flags & ~static_cast<int>(SV_ATTN_EARLY_CONTEXT)) != 0)
     return SV_ERR_INVALID_ARG;
   if (p->num_q_heads % p->num_kv_heads != 0) return SV_ERR_INVALID_ARG;
   const int G = p->num_q_heads / p->num_kv_heads;
@@ -756,7 +803,6 @@ sv_status validate(const sv_attn_params* p) {
   if (p->page_size != 16) return SV_ERR_UNSUPPORTED;
   if (p->max_nodes > kMaxNodes) return SV_ERR_UNSUPPORTED;
   if (p->num_splits > kMaxSplits) return SV_ERR_UNSUPPORTED;
-  if (p->split_reduce == 1 && p->num_splits > kMaxClusterSplits) return SV_ERR_UNSUPPORTED;
   if (!p->q || !p->tree_k || !p->tree_v || !p->k_cache || !p->v_cache || !p->block_table || !p->ctx_lens ||
       !p->cu_nodes || !p->parents || !p->out)
     return SV_ERR_INVALID_ARG;
@@ -764,13 +810,14 @@ sv_status validate(const sv_attn_params* p) {
   if (!aligned16(p->q) || !aligned16(p->tree_k) || !aligned16(p->tree_v) || !aligned16(p->k_cache) ||
       !aligned16(p->v_cache) || !aligned16(p->out))
     return SV_ERR_INVALID_ARG;
-  if (static_cast<long long>(p->batch) * p->num_kv_heads * ((p->max_nodes * G + kCtaRows - 1) / kCtaRows) > 65535)
+  const long long row_tiles = (static_cast<long long>(p->max_nodes) * G + kTileRows - 1) / kTileRows;
+  if (static_cast<long long>(p->num_kv_heads) * (row_tiles + 1) > 65535 || p->batch > 65535)
     return SV_ERR_UNSUPPORTED;
   return SV_OK;
 }
 
 template <int D>
-void launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attrs, dim3 grid, int cluster, cudaStream_t s) {
+void launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attrs, dim3 grid, bool paired, cudaStream_t s) {
   *cfg = cudaLaunchConfig_t{};
   cfg->gridDim = grid;
   cfg->blockDim = dim3(kThreads, 1, 1);
@@ -780,10 +827,10 @@ void launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attrs, dim3 gri
   attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attrs[n].val.programmaticStreamSerializationAllowed = 1;
   ++n;
-  if (cluster > 1) {
+  if (paired) {
     attrs[n].id = cudaLaunchAttributeClusterDimension;
-    attrs[n].val.clusterDim.x = cluster;
-    attrs[n].val.clusterDim.y = 1;
+    attrs[n].val.clusterDim.x = 1;
+    attrs[n].val.clusterDim.y = 2;
     attrs[n].val.clusterDim.z = 1;
     ++n;
   }
@@ -791,7 +838,7 @@ void launch_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attrs, dim3 gri
   cfg->numAttrs = n;
 }
 
-// One-time per-device kernel attributes (dynamic smem, cluster size > 8).
+// One-time per-device kernel attribute (dynamic shared memory size).
 template <int D>
 bool configure_kernel() {
   static std::mutex mu;
@@ -803,112 +850,84 @@ bool configure_kernel() {
   if (cudaFuncSetAttribute(tree_attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<D>::kSmemBytes) != cudaSuccess)
     return false;
-  if (cudaFuncSetAttribute(tree_attention_kernel<D>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-      cudaSuccess)
-    return false;
   if (dev < 64) done[dev] = true;
   return true;
 }
 
-// Co-resident clusters of `size` CTAs at this kernel's footprint (cached per
-// device); 0 when they cannot be scheduled or the query fails.
+// Co-resident CTA pairs at this kernel's footprint (cached per device; a pair
+// needs two SMs of one GPC); 0 when the query fails.
 template <int D>
-int max_active_clusters(int size) {
+int max_active_pairs() {
   static std::mutex mu;
-  static int cache[64][kMaxClusterSplits + 1];
+  static int cache[64];
   static bool init = false;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
   if (!init) {
-    for (auto& row : cache)
-      for (int& v : row) v = -1;
+    for (int& v : cache) v = -1;
     init = true;
   }
-  if (cache[dev][size] >= 0) return cache[dev][size];
+  if (cache[dev] >= 0) return cache[dev];
   int n = 0;
   if (configure_kernel<D>()) {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attrs[2];
-    launch_config<D>(&cfg, attrs, dim3(size, 1, 1), size, nullptr);
+    launch_config<D>(&cfg, attrs, dim3(1, 2, 1), true, nullptr);
     if (cudaOccupancyMaxActiveClusters(&n, tree_attention_kernel<D>, &cfg) != cudaSuccess) n = 0;
   }
   cudaGetLastError();
-  cache[dev][size] = n;
+  cache[dev] = n;
   return n;
 }
 
-int active_clusters(int head_dim, int size) {
-  return head_dim == 128 ? max_active_clusters<128>(size) : max_active_clusters<64>(size);
-}
-
-// Split count and merge mode from a small cost model in units of one KV tile
-// of work: a CTA costs its share of tiles plus a fixed prologue/epilogue;
-// waves come from how many CTAs (or clusters) are co-resident; an on-chip
-// merge costs a little per CTA, a global merge costs partial writes plus a
-// second kernel.
-void choose_splits(const sv_attn_params* p, int sms, int groups_per_seq, int* splits, int* mode) {
-  const long long units = static_cast<long long>(p->batch) * p->num_kv_heads * groups_per_seq;
+// Split count from a small cost model in units of one K/V tile of work per
+// CTA: a CTA costs its share of tiles plus a fixed prologue, first-load and
+// epilogue cost; waves come from how many CTAs are co-resident (one per SM,
+// pairs within a GPC); splitting adds partial writes and the combine kernel.
+int choose_splits(const sv_attn_params* p, int slots, int units) {
   const int pages = p->kv_pages ? p->max_kv_pages : p->max_pages_per_seq;
   const int tiles = (pages + kPagesPerTile - 1) / kPagesPerTile + 1;
-  // merge costs measured on GB300 (in tiles of work): the in-cluster merge is
-  // latency-bound (~5 us); partial writes ~1 tile; the combine kernel ~2
-  const double c_cta = 1.5, c_red = 4.0, c_part = 1.0, c_comb = 2.0;
-  auto cost_cluster = [&](int s) -> double {
-    const int act = active_clusters(p->head_dim, s);
-    if (act <= 0) return 1e300;
-    const long long waves = (units + act - 1) / act;
-    return static_cast<double>(waves) * (static_cast<double>((tiles + s - 1) / s) + c_cta + c_red);
+  const double c_cta = 6.0, c_part = 1.0, c_comb = 4.0;
+  auto cost = [&](int s) -> double {
+    const long long ctas = static_cast<long long>(units) * s;
+    const long long waves = (ctas + slots - 1) / slots;
+    double c = static_cast<double>(waves) * (static_cast<double>((tiles + s - 1) / s) + c_cta);
+    if (s > 1) c += static_cast<double>(waves) * c_part + c_comb + 0.05 * s;
+    return c;
   };
-  auto cost_global = [&](int s) -> double {
-    const long long waves = (units * s + sms - 1) / sms;
-    return static_cast<double>(waves) * (static_cast<double>((tiles + s - 1) / s) + c_cta + c_part) + c_comb +
-           0.05 * s;
-  };
-  if (p->num_splits > 0) {
-    *splits = p->num_splits;
-    if (*splits == 1) *mode = kReduceNone;
-    else if (p->split_reduce == 2) *mode = kReduceGlobal;
-    else if (p->split_reduce == 1) *mode = kReduceCluster;
-    else *mode = (*splits <= 8 || (*splits <= kMaxClusterSplits && sms > 0 && active_clusters(p->head_dim, *splits) > 0))
-                     ? kReduceCluster : kReduceGlobal;
-    return;
-  }
-  const long long waves1 = (units + sms - 1) / sms;
-  double best = static_cast<double>(waves1) * (tiles + c_cta);
-  *splits = 1;
-  *mode = kReduceNone;
+  int best_s = 1;
+  double best = cost(1);
   for (int s = 2; s <= kMaxSplits && s <= tiles; ++s) {
-    if (p->split_reduce != 2 && s <= kMaxClusterSplits) {
-      const double c = cost_cluster(s);
-      if (c < best - 1e-9) {
-        best = c;
-        *splits = s;
-        *mode = kReduceCluster;
-      }
-    }
-    if (p->split_reduce != 1) {
-      const double c = cost_global(s);
-      if (c < best - 1e-9) {
-        best = c;
-        *splits = s;
-        *mode = kReduceGlobal;
-      }
+    const double c = cost(s);
+    if (c < best - 1e-9) {
+      best = c;
+      best_s = s;
     }
   }
+  return best_s;
 }
 
 sv_status make_plan(const sv_attn_params* p, Plan* plan) {
   sv_status st = validate(p);
   if (st != SV_OK) return st;
   plan->group = p->num_q_heads / p->num_kv_heads;
-  plan->groups_per_seq = (p->max_nodes * plan->group + kCtaRows - 1) / kCtaRows;
-  int sms = 0;
-  if (p->num_splits == 0 || (p->num_splits > 8 && p->split_reduce == 0)) {
-    sms = device_sm_count();
+  const int rt = (p->max_nodes * plan->group + kTileRows - 1) / kTileRows;
+  plan->paired = rt >= 2 ? 1 : 0;
+  plan->row_tiles = plan->paired ? (rt + 1) / 2 * 2 : rt;
+  if (p->num_splits > 0) {
+    plan->splits = p->num_splits;
+  } else {
+    const int sms = device_sm_count();
     if (sms <= 0) return SV_ERR_CUDA;
+    int slots = sms;
+    if (plan->paired) {
+      const int pairs = p->head_dim == 128 ? max_active_pairs<128>() : max_active_pairs<64>();
+      if (pairs > 0) slots = 2 * pairs;
+    }
+    plan->splits = choose_splits(p, slots, p->batch * p->num_kv_heads * plan->row_tiles);
   }
-  choose_splits(p, sms, plan->groups_per_seq, &plan->splits, &plan->mode);
+  plan->mode = plan->splits > 1 ? kReduceGlobal : kReduceNone;
   size_t ws = kWorkspaceHeader;
   if (plan->mode != kReduceNone) {
     const size_t rows = static_cast<size_t>(p->total_nodes) * p->num_q_heads;
@@ -924,16 +943,8 @@ sv_status launch(const sv_attn_params* p, const Plan& plan, cudaStream_t stream)
   if (!configure_kernel<D>()) return SV_ERR_CUDA;
   const int G = plan.group;
   const cuuint64_t T = static_cast<cuuint64_t>(p->total_nodes);
-  const cuuint64_t Hq = p->num_q_heads, Hkv = p->num_kv_heads, Dd = D, P = p->page_size;
-  CUtensorMap tm_q, tm_kc, tm_vc, tm_tk, tm_tv;
-  {
-    const cuuint64_t dims[3] = {Dd, Hq, T};
-    const cuuint64_t strides[2] = {Dd * 2, Hq * Dd * 2};
-    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(kTileRows / G)};
-    if (encode_tiled(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(p->q), dims, strides, box,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B) != CUDA_SUCCESS)
-      return SV_ERR_CUDA;
-  }
+  const cuuint64_t Hkv = p->num_kv_heads, Dd = D, P = p->page_size;
+  CUtensorMap tm_kc, tm_vc, tm_tk, tm_tv;
   {
     const cuuint64_t dims[4] = {Dd, P, Hkv, static_cast<cuuint64_t>(p->num_pages)};
     const cuuint64_t strides[3] = {Dd * 2, P * Dd * 2, Hkv * P * Dd * 2};
@@ -964,6 +975,10 @@ sv_status launch(const sv_attn_params* p, const Plan& plan, cudaStream_t stream)
   kp.parents = p->parents;
   kp.kv_pages = p->kv_pages;
   kp.cu_kv_pages = p->cu_kv_pages;
+  kp.q = static_cast<const __nv_bfloat16*>(p->q);
+  kp.k_cache = static_cast<const __nv_bfloat16*>(p->k_cache);
+  kp.v_cache = static_cast<const __nv_bfloat16*>(p->v_cache);
+  kp.num_kv_heads = p->num_kv_heads;
   kp.out = static_cast<__nv_bfloat16*>(p->out);
   kp.lse = p->lse;
   kp.err = reinterpret_cast<int*>(ws);
@@ -984,24 +999,31 @@ sv_status launch(const sv_attn_params* p, const Plan& plan, cudaStream_t stream)
   kp.group = G;
   kp.num_pages = p->num_pages;
   kp.max_pages_per_seq = p->max_pages_per_seq;
+  kp.max_nodes = p->max_nodes;
   kp.num_splits = plan.splits;
   kp.reduce_mode = plan.mode;
+  kp.early_ctx = (p->flags & SV_ATTN_EARLY_CONTEXT) ? 1 : 0;
   kp.total_nodes = p->total_nodes;
-  kp.groups_per_seq = plan.groups_per_seq;
+  kp.row_tiles = plan.row_tiles;
+  kp.paired = plan.paired;
   const float scale = (p->sm_scale > 0.f) ? p->sm_scale : 1.0f / sqrtf(static_cast<float>(D));
   kp.scale_log2 = scale * 1.4426950408889634f;
 
   cudaLaunchConfig_t cfg;
   cudaLaunchAttribute attrs[2];
-  launch_config<D>(&cfg, attrs, dim3(plan.splits, p->num_kv_heads * plan.groups_per_seq, p->batch),
-                   plan.mode == kReduceCluster ? plan.splits : 1, stream);
-  if (cudaLaunchKernelEx(&cfg, tree_attention_kernel<D>, tm_q, tm_kc, tm_vc, tm_tk, tm_tv, kp) != cudaSuccess)
+  launch_config<D>(&cfg, attrs, dim3(plan.splits, p->num_kv_heads * plan.row_tiles, p->batch), plan.paired != 0,
+                   stream);
+  if (cudaLaunchKernelEx(&cfg, tree_attention_kernel<D>, tm_kc, tm_vc, tm_tk, tm_tv, kp) != cudaSuccess)
     return SV_ERR_CUDA;
   if (plan.mode == kReduceGlobal) {
-    const int blocks = static_cast<int>((rows * 32 + 255) / 256);
-    split_combine_kernel<D><<<blocks, 256, 0, stream>>>(kp.part_o, kp.part_lse, kp.out, p->lse,
-                                                         static_cast<int>(rows), plan.splits);
-    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    cudaLaunchConfig_t ccfg = cudaLaunchConfig_t{};
+    ccfg.gridDim = dim3(static_cast<unsigned>((rows * 32 + 255) / 256), 1, 1);
+    ccfg.blockDim = dim3(256, 1, 1);
+    ccfg.stream = stream;
+    if (cudaLaunchKernelEx(&ccfg, split_combine_kernel<D>, static_cast<const __nv_bfloat16*>(kp.part_o),
+                           static_cast<const float*>(kp.part_lse), kp.out, p->lse, static_cast<int>(rows),
+                           plan.splits) != cudaSuccess)
+      return SV_ERR_CUDA;
   }
   return SV_OK;
 }

@@ -49,7 +49,7 @@ class DeviceCase:
 
 def run_attention(dc: DeviceCase, li: int = 0, partial: bool = False, num_splits: int = 0,
                   with_lse: bool = True, sm_scale: float = 0.0, check_error: bool = True,
-                  split_reduce: int = 0):
+                  split_reduce: int = 0, flags: int = 0):
     c = dc.case
     T, Hq, D = c.total_nodes, c.num_q_heads, c.head_dim
     out = torch.full((T, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
@@ -62,7 +62,7 @@ def run_attention(dc: DeviceCase, li: int = 0, partial: bool = False, num_splits
         v_cache=dc.v_cache[li], block_table=dc.block_table, ctx_lens=dc.ctx_lens, cu_nodes=dc.cu_nodes,
         parents=dc.parents, out=out, lse=lse, total_nodes=T, max_nodes=c.max_nodes,
         kv_pages=kvp, cu_kv_pages=ckvp, max_kv_pages=max_kv, num_splits=num_splits, sm_scale=sm_scale,
-        split_reduce=split_reduce)
+        split_reduce=split_reduce, flags=flags)
     ws_bytes = binding.sv_tree_attention_workspace_size(p)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
     p.workspace = ws.data_ptr()

@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert binding.sv_abi_version() == 1
+    assert binding.sv_abi_version() == 2
     for code in range(7):
         s = binding.sv_status_string(code)
         assert s.startswith(binding.STATUS_NAMES[code])
@@ -71,6 +71,8 @@ def _fake_params(**over):
     (dict(workspace_bytes=16), 4),
     (dict(kv_pages=1 << 20), 1),                     # list without prefix sums
     (dict(batch=0), 1),
+    (dict(split_reduce=1), 1),                       # only 0 (auto) and 2 (partials) exist
+    (dict(flags=2), 1),                              # unknown option bit
 ])
 def test_attention_host_validation(lib, over, status):
     p = _fake_params(**over)

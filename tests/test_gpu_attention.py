@@ -12,6 +12,7 @@ import torch
 
 import oracle
 from synth import make_case, tree_chain
+from speculative_decoding_tree_sv_gb300 import binding
 from tests.gpu_support import ATOL_ATTN, ATOL_LSE, DeviceCase, ensure_lib, run_attention
 
 pytestmark = pytest.mark.gpu
@@ -43,27 +44,70 @@ def _compare(case, out, lse, ref, ref_lse, seqs=None, kv_heads=None):
         assert dl.max() <= ATOL_LSE, f"max |lse diff| = {dl.max()}"
 
 
-def _check(case, partial=False, num_splits=0, seqs=None, kv_heads=None, sm_scale=0.0, li=0, split_reduce=0):
+def _check(case, partial=False, num_splits=0, seqs=None, kv_heads=None, sm_scale=0.0, li=0, split_reduce=0,
+           flags=0):
     dc = DeviceCase(case, layers=[li])
     out, lse, _ = run_attention(dc, 0, partial=partial, num_splits=num_splits, sm_scale=sm_scale,
-                                split_reduce=split_reduce)
+                                split_reduce=split_reduce, flags=flags)
     ref, ref_lse = _oracle(case, li, partial, seqs, kv_heads, sm_scale=sm_scale if sm_scale > 0 else None)
     _compare(case, out, lse, ref, ref_lse, seqs, kv_heads)
     return out
 
 
-@pytest.mark.parametrize("splits,mode", [(0, 0), (1, 0), (2, 1), (5, 1), (5, 2), (7, 1)])
+@pytest.mark.parametrize("splits,mode", [(0, 0), (1, 0), (2, 2), (5, 2), (7, 2)])
 def test_tiny(splits, mode):
     # more splits than tiles leaves some splits empty
     _check(make_case("tiny"), num_splits=splits, split_reduce=mode)
 
 
-@pytest.mark.parametrize("splits,mode", [(0, 0), (1, 0), (3, 1), (3, 2), (10, 1), (16, 1), (19, 2), (34, 2),
-                                         (2, 1), (9, 1)])
+@pytest.mark.parametrize("splits,mode", [(0, 0), (1, 0), (2, 2), (3, 2), (9, 2), (10, 2), (16, 2), (19, 2),
+                                         (34, 2)])
 def test_llama_eagle_layer(splits, mode):
-    # mode 1: splits merged on chip through the cluster's shared memory;
-    # mode 2: through workspace partials and a combine kernel
+    # 240 rows per KV head: a CTA pair shares every K/V tile; splits merge
+    # through workspace partials and a combine kernel
     _check(make_case("llama8b_eagle", layers=1, with_logits=False), num_splits=splits, split_reduce=mode)
+
+
+@pytest.mark.parametrize("splits,mode", [(0, 0), (1, 0), (3, 2), (5, 2), (33, 2)])
+def test_early_context_flag(splits, mode):
+    # the context pages and index arrays are read before the wait on the
+    # preceding grid; results are unchanged
+    _check(make_case("llama8b_eagle", layers=1, with_logits=False), num_splits=splits, split_reduce=mode,
+           flags=binding.SV_ATTN_EARLY_CONTEXT)
+    _check(make_case("tiny", batch=3, ctx=[0, 33, 200], with_logits=False, seed=5), num_splits=splits,
+           split_reduce=mode, flags=binding.SV_ATTN_EARLY_CONTEXT)
+
+
+def test_early_context_back_to_back_layers():
+    # consecutive launches on one stream overlap; every layer must still see
+    # its own Q and write its own output
+    case = make_case("llama8b_eagle", layers=4, with_logits=False)
+    dc = DeviceCase(case)
+    c = case
+    outs = []
+    ws = None
+    params = []
+    for li in range(4):
+        out = torch.empty((c.total_nodes, c.num_q_heads, c.head_dim), dtype=torch.bfloat16, device="cuda")
+        p = binding.make_attn_params(
+            q=dc.q[li], tree_k=dc.tree_k[li], tree_v=dc.tree_v[li], k_cache=dc.k_cache[li],
+            v_cache=dc.v_cache[li], block_table=dc.block_table, ctx_lens=dc.ctx_lens, cu_nodes=dc.cu_nodes,
+            parents=dc.parents, out=out, total_nodes=c.total_nodes, max_nodes=c.max_nodes,
+            flags=binding.SV_ATTN_EARLY_CONTEXT)
+        if ws is None:
+            ws = torch.zeros(binding.sv_tree_attention_workspace_size(p), dtype=torch.uint8, device="cuda")
+        p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
+        params.append(p)
+        outs.append(out)
+    for _ in range(3):
+        for p in params:
+            binding.sv_tree_attention(p)
+    torch.cuda.synchronize()
+    assert binding.sv_get_device_error(ws) == 0
+    for li in range(4):
+        ref, _ = _oracle(case, li)
+        diff = np.abs(outs[li].float().cpu().numpy() - ref).max()
+        assert diff <= ATOL_ATTN, (li, diff)
 
 
 def test_serving_mix_full_batch():
@@ -73,9 +117,9 @@ def test_serving_mix_full_batch():
 def test_long_context_partial_and_full():
     case = make_case("long_partial", with_logits=False)
     _check(case, partial=True)
-    _check(case, partial=True, num_splits=12, split_reduce=1)
+    _check(case, partial=True, num_splits=12, split_reduce=2)
     _check(case, partial=False, kv_heads=[0, 5])
-    _check(case, partial=False, kv_heads=[3], num_splits=16, split_reduce=1)
+    _check(case, partial=False, kv_heads=[3], num_splits=16, split_reduce=2)
 
 
 def test_specblock_sampled():
@@ -172,11 +216,16 @@ def test_bad_page_is_reported_not_trapped():
 
 
 @pytest.mark.parametrize("nodes", [1, 2, 32])
-@pytest.mark.parametrize("splits", [4, 8])
-def test_single_row_tile_with_on_chip_merge(nodes, splits):
-    # only the first 128-row tile is active: the idle softmax group must not
-    # touch the merge buffer (it overlays the K/V stages) before the MMAs end
-    par = [-1] + list(range(nodes - 1))
-    case = make_case("llama8b_eagle", layers=1, ctx=777, parents_list=[par], with_logits=False)
-    for _ in range(3):
-        _check(case, num_splits=splits, split_reduce=1)
+@pytest.mark.parametrize("splits", [0, 1, 4])
+def test_pair_with_an_empty_row_tile(nodes, splits):
+    # the 60-node tree needs two 128-row tiles (a CTA pair sharing each K/V
+    # tile); the small tree of the other sequence leaves the second CTA of
+    # its pair without rows, and that CTA must still load and release its
+    # half of every tile
+    rng = np.random.default_rng(nodes)
+    big = [-1] + [int(rng.integers(0, i)) for i in range(1, 60)]
+    small = [-1] + list(range(nodes - 1))
+    case = make_case("llama8b_eagle", layers=1, batch=2, ctx=[777, 300], parents_list=[big, small],
+                     with_logits=False, seed=nodes + 11)
+    for _ in range(2):
+        _check(case, num_splits=splits, split_reduce=2 if splits > 1 else 0)
