@@ -220,7 +220,7 @@ class GpuStep:
         self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
         for p in self.params:
             p.workspace, p.workspace_bytes = self.ws.data_ptr(), ws_bytes
-        self.splits, self.split_reduce = binding.sv_tree_attention_plan(self.params[0])
+        self.splits, self.split_reduce, self.kernel = binding.sv_tree_attention_plan(self.params[0], with_kernel=True)
         B = c.batch
         self.am = torch.empty(self.T, dtype=torch.int32, device=dev)
         self.alen = torch.empty(B, dtype=torch.int32, device=dev)
@@ -420,7 +420,8 @@ def run_gpu(args):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOADS[args.config], "layers": c.num_layers, "batch": c.batch,
                        "total_nodes": c.total_nodes, "kv_splits": st.splits,
-                       "split_merge": ["none", "on-chip cluster", "global partials"][st.split_reduce],
+                       "split_merge": "combine kernel" if st.split_reduce == 2 else "none",
+                       "attention_kernel": ["paired 128-row CTAs", "256-row CTAs"][st.kernel],
                        "cuda_graph": True, "early_context": bool(flags),
                        "l2": "inputs larger than L2 (distinct KV per layer, %.0f MB per step)"
                              % (sum(ctx_keys) * 4 * c.num_kv_heads * c.head_dim * c.num_layers / 1e6),

@@ -106,7 +106,16 @@ const char* sv_status_string(sv_status status);
  * completion (griddepcontrol.launch_dependents) before writing them; the
  * kernels of this library never write them.  Consecutive layers then
  * overlap one layer's context loads with the previous layer's tail. */
-enum sv_attn_flags { SV_ATTN_EARLY_CONTEXT = 1 };
+enum sv_attn_flags {
+  SV_ATTN_EARLY_CONTEXT = 1,
+  /* Kernel choice (at most one; by default a cost model picks).  PAIRED: one
+   * CTA per 128-row tile, the two row tiles of a group share each K/V tile
+   * by cluster multicast, scores double-buffered in TMEM; suits short
+   * contexts split across many CTAs.  WIDE: one CTA per 256-row group, each
+   * K/V tile staged in one SM only; suits long and batched contexts. */
+  SV_ATTN_KERNEL_PAIRED = 2,
+  SV_ATTN_KERNEL_WIDE = 4
+};
 
 typedef struct sv_attn_params {
   /* shapes (host values) */
@@ -121,11 +130,9 @@ typedef struct sv_attn_params {
   int max_pages_per_seq;  /* row length of block_table                       */
   int max_kv_pages;       /* partial mode: max_b listed pages (host copy)    */
   int num_splits;         /* KV splits per (sequence, head group); 0 = auto  */
-  int split_reduce;       /* how splits merge: 0 = auto, 1 = on chip (the
-                             splits form a thread-block cluster and merge
-                             through distributed shared memory; num_splits
-                             <= 16), 2 = through workspace partials and a
-                             second kernel                                   */
+  int split_reduce;       /* how splits merge: 0 = auto, 2 = through
+                             workspace partials and a combine kernel (the
+                             only merge; other values are rejected)          */
   float sm_scale;         /* softmax scale; <= 0 selects 1/sqrt(D)           */
   int flags;              /* bitwise OR of sv_attn_flags, 0 for none         */
 
@@ -156,13 +163,15 @@ typedef struct sv_attn_params {
 sv_status sv_tree_attention_workspace_size(const sv_attn_params* params, size_t* bytes);
 
 /* The launch plan sv_tree_attention would use for these parameters: the
- * number of KV splits and how they merge (0 = single split, 1 = on chip
- * through the cluster's shared memory, 2 = through workspace partials). */
-sv_status sv_tree_attention_plan(const sv_attn_params* params, int* num_splits, int* split_reduce);
+ * number of KV splits, how they merge (0 = single split, 2 = through
+ * workspace partials and the combine kernel) and, if kernel is non-NULL,
+ * the kernel (0 = paired, 1 = wide; see sv_attn_flags). */
+sv_status sv_tree_attention_plan(const sv_attn_params* params, int* num_splits, int* split_reduce, int* kernel);
 
 /* Launches the attention (and, with more than one split, the split combine)
- * on `stream`.  Grid: one CTA per (KV split, KV head x 256-row group,
- * sequence); see the library's design notes for the kernel. */
+ * on `stream`: one CTA per (KV split, KV head x 128-row tile, sequence) for
+ * the paired kernel or per (KV split, KV head x 256-row group, sequence) for
+ * the wide one (sv_attn_flags). */
 sv_status sv_tree_attention(const sv_attn_params* params, sv_stream_t stream);
 
 /* ------------------------------------------------------------------------

@@ -21,6 +21,8 @@ SV_OK = 0
 STATUS_NAMES = {0: "SV_OK", 1: "SV_ERR_INVALID_ARG", 2: "SV_ERR_UNSUPPORTED", 3: "SV_ERR_CUDA",
                 4: "SV_ERR_WORKSPACE", 5: "SV_ERR_DEVICE", 6: "SV_ERR_TIMEOUT"}
 SV_ATTN_EARLY_CONTEXT = 1
+SV_ATTN_KERNEL_PAIRED = 2
+SV_ATTN_KERNEL_WIDE = 4
 DEVICE_ERRORS = {0: "none", 1: "timeout", 2: "bad parent", 3: "bad page", 4: "bad path", 5: "depth",
                  6: "bad tree"}
 
@@ -66,7 +68,7 @@ def load(path: Optional[str] = None):
     lib.sv_tree_attention_workspace_size.restype = c_int
     lib.sv_tree_attention_workspace_size.argtypes = [P(sv_attn_params), P(c_size_t)]
     lib.sv_tree_attention_plan.restype = c_int
-    lib.sv_tree_attention_plan.argtypes = [P(sv_attn_params), P(c_int), P(c_int)]
+    lib.sv_tree_attention_plan.argtypes = [P(sv_attn_params), P(c_int), P(c_int), P(c_int)]
     lib.sv_tree_attention.restype = c_int
     lib.sv_tree_attention.argtypes = [P(sv_attn_params), c_void_p]
     lib.sv_greedy_accept_workspace_size.restype = c_int
@@ -161,11 +163,14 @@ def sv_tree_attention_workspace_size(params: sv_attn_params) -> int:
     return int(n.value)
 
 
-def sv_tree_attention_plan(params: sv_attn_params):
-    """(num_splits, split_reduce) the library would launch with."""
-    s, m = c_int(0), c_int(0)
-    _check(load().sv_tree_attention_plan(ctypes.byref(params), ctypes.byref(s), ctypes.byref(m)),
+def sv_tree_attention_plan(params: sv_attn_params, with_kernel: bool = False):
+    """(num_splits, split_reduce) the library would launch with, plus the
+    kernel (0 = paired, 1 = wide) when with_kernel is set."""
+    s, m, k = c_int(0), c_int(0), c_int(0)
+    _check(load().sv_tree_attention_plan(ctypes.byref(params), ctypes.byref(s), ctypes.byref(m), ctypes.byref(k)),
            "sv_tree_attention_plan")
+    if with_kernel:
+        return int(s.value), int(m.value), int(k.value)
     return int(s.value), int(m.value)
 
 

@@ -33,4 +33,18 @@ CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, cuuint32_t ra
 // Number of SMs of the current device (cached per device); -1 on failure.
 int device_sm_count();
 
+// The 256-row attention kernel (tree_attention_wide.cu): one CTA per (KV
+// split, KV head x 256-row group, sequence).  With splits > 1 it writes
+// partials (bf16 O / l at part_o, log2-sum-exp at part_lse, [splits][T * Hq])
+// for the combine kernel; err is the workspace's error word.
+struct WideLaunch {
+  int splits;
+  void* part_o;
+  float* part_lse;
+  int* err;
+  unsigned long long* trace;
+  long long trace_ctas;
+};
+sv_status launch_wide_attention(const sv_attn_params* p, const WideLaunch& w, cudaStream_t stream);
+
 }  // namespace sv

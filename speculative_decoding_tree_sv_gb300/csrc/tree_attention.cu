@@ -224,7 +224,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // first; with early_ctx the index arrays and context pages are read
   // before that wait.
   if (!p.early_ctx) griddep_wait();
-  griddep_launch_dependents();
+  // Without a split merge the next grid is the next attention call: let it
+  // start its prologue now.  With one, the next grid is the combine kernel,
+  // which is only useful once the partials are written (signalled at exit).
+  if (p.reduce_mode == kReduceNone) griddep_launch_dependents();
   if (threadIdx.x == 0) mark(SV_TRACE_INPUTS);
 
   const int n0 = p.cu_nodes[b];
@@ -691,6 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (p.reduce_mode != kReduceNone) griddep_launch_dependents();
   // neither CTA of a pair leaves while the other may still address its
   // shared memory (multicast copies, remote arrives); every path of both CTAs
   // reaches this point, since every other wait is bounded
@@ -705,9 +709,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Merge split partials: O = sum_s w_s O_s / sum_s w_s, w_s = 2^(lse_s - max).
 // One warp per output row: lane s holds split s's (and s + 32's) log2-sum-exp,
 // the weights come from warp reductions, and the partial rows are read eight
-// splits at a time so their loads overlap.  It lets the next grid in the
-// stream launch early (programmatic dependent launch): a following attention
-// grid then runs its prologue while this one merges.
+// splits at a time so their loads overlap.  It is launched as a programmatic
+// dependent of the attention grid (whose CTAs signal once their partials are
+// written) and lets the next grid in the stream launch early in turn.
 template <int D>
 __global__ void __launch_bounds__(256) split_combine_kernel(const __nv_bfloat16* __restrict__ part_o,
                                                             const float* __restrict__ part_lse,
@@ -784,6 +788,7 @@ struct Plan {
   int group;
   int row_tiles;
   int paired;
+  int wide;  // 1: the 256-row kernel (tree_attention_wide.cu)
   int splits;
   int mode;
   size_t workspace;
@@ -794,7 +799,8 @@ sv_status validate(const sv_attn_params* p) {
   if (p->batch < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1 || p->total_nodes < 0 || p->max_nodes < 1 ||
       p->max_pages_per_seq < 1 || p->num_pages < 1 || p->num_splits < 0 || p->max_kv_pages < 0 ||
       (p->split_reduce != 0 && p->split_reduce != 2) ||
-      (p->flags & ~static_cast<int>(SV_ATTN_EARLY_CONTEXT)) != 0)
+      (p->flags & ~static_cast<int>(SV_ATTN_EARLY_CONTEXT | SV_ATTN_KERNEL_PAIRED | SV_ATTN_KERNEL_WIDE)) != 0 ||
+      ((p->flags & SV_ATTN_KERNEL_PAIRED) && (p->flags & SV_ATTN_KERNEL_WIDE)))
     return SV_ERR_INVALID_ARG;
   if (p->num_q_heads % p->num_kv_heads != 0) return SV_ERR_INVALID_ARG;
   const int G = p->num_q_heads / p->num_kv_heads;
@@ -881,30 +887,42 @@ int max_active_pairs() {
   return n;
 }
 
-// Split count from a small cost model in units of one K/V tile of work per
-// CTA: a CTA costs its share of tiles plus a fixed prologue, first-load and
-// epilogue cost; waves come from how many CTAs are co-resident (one per SM,
-// pairs within a GPC); splitting adds partial writes and the combine kernel.
-int choose_splits(const sv_attn_params* p, int slots, int units) {
-  const int pages = p->kv_pages ? p->max_kv_pages : p->max_pages_per_seq;
-  const int tiles = (pages + kPagesPerTile - 1) / kPagesPerTile + 1;
-  const double c_cta = 6.0, c_part = 1.0, c_comb = 4.0;
-  auto cost = [&](int s) -> double {
-    const long long ctas = static_cast<long long>(units) * s;
-    const long long waves = (ctas + slots - 1) / slots;
-    double c = static_cast<double>(waves) * (static_cast<double>((tiles + s - 1) / s) + c_cta);
-    if (s > 1) c += static_cast<double>(waves) * c_part + c_comb + 0.05 * s;
-    return c;
-  };
+// Kernel and split count from a small cost model, in microseconds measured
+// on GB300: a CTA costs a fixed prologue, first-load and epilogue time plus
+// its share of K/V tiles (128 keys); waves come from how many CTAs are
+// co-resident (one per SM; pairs within a GPC); splitting adds the combine
+// kernel.  The paired kernel streams a tile per 128 rows in ~1.25 us, the
+// 256-row kernel per 256 rows in ~2.1 us, with fixed costs of ~6.5 and
+// ~8.5 us.
+struct KernelCost {
+  double fixed, per_tile;
+  int slots;  // co-resident CTAs
+  long long units;  // CTAs per split
+};
+
+double plan_cost(const KernelCost& k, int tiles, int s) {
+  const long long ctas = k.units * s;
+  const long long waves = (ctas + k.slots - 1) / k.slots;
+  double c = static_cast<double>(waves) * (k.fixed + k.per_tile * ((tiles + s - 1) / s));
+  if (s > 1) c += 5.0 + 0.05 * s;
+  return c;
+}
+
+int best_splits(const KernelCost& k, int tiles, int fixed_splits, double* cost) {
+  if (fixed_splits > 0) {
+    *cost = plan_cost(k, tiles, fixed_splits);
+    return fixed_splits;
+  }
   int best_s = 1;
-  double best = cost(1);
+  double best = plan_cost(k, tiles, 1);
   for (int s = 2; s <= kMaxSplits && s <= tiles; ++s) {
-    const double c = cost(s);
+    const double c = plan_cost(k, tiles, s);
     if (c < best - 1e-9) {
       best = c;
       best_s = s;
     }
   }
+  *cost = best;
   return best_s;
 }
 
@@ -915,18 +933,31 @@ sv_status make_plan(const sv_attn_params* p, Plan* plan) {
   const int rt = (p->max_nodes * plan->group + kTileRows - 1) / kTileRows;
   plan->paired = rt >= 2 ? 1 : 0;
   plan->row_tiles = plan->paired ? (rt + 1) / 2 * 2 : rt;
-  if (p->num_splits > 0) {
-    plan->splits = p->num_splits;
-  } else {
-    const int sms = device_sm_count();
-    if (sms <= 0) return SV_ERR_CUDA;
-    int slots = sms;
-    if (plan->paired) {
-      const int pairs = p->head_dim == 128 ? max_active_pairs<128>() : max_active_pairs<64>();
-      if (pairs > 0) slots = 2 * pairs;
+  const int pages = p->kv_pages ? p->max_kv_pages : p->max_pages_per_seq;
+  const int tiles = (pages + kPagesPerTile - 1) / kPagesPerTile + 1;
+  const bool force_paired = (p->flags & SV_ATTN_KERNEL_PAIRED) != 0;
+  const bool force_wide = (p->flags & SV_ATTN_KERNEL_WIDE) != 0;
+  // With an explicit split count the workspace does not depend on the
+  // device, so host-only queries fall back to GB300's figures.
+  int sms = 152, pairs = 76;
+  if (p->num_splits == 0 || (!force_paired && !force_wide)) {
+    const int n = device_sm_count();
+    if (n > 0) {
+      sms = n;
+      pairs = plan->paired ? (p->head_dim == 128 ? max_active_pairs<128>() : max_active_pairs<64>()) : 0;
+    } else if (p->num_splits == 0) {
+      return SV_ERR_CUDA;
     }
-    plan->splits = choose_splits(p, slots, p->batch * p->num_kv_heads * plan->row_tiles);
   }
+  KernelCost kp{6.5, 1.25, plan->paired && pairs > 0 ? 2 * pairs : sms,
+                static_cast<long long>(p->batch) * p->num_kv_heads * plan->row_tiles};
+  KernelCost kw{8.5, 2.1, sms,
+                static_cast<long long>(p->batch) * p->num_kv_heads * ((p->max_nodes * plan->group + 255) / 256)};
+  double cost_p = 0, cost_w = 0;
+  const int sp = best_splits(kp, tiles, p->num_splits, &cost_p);
+  const int sw = best_splits(kw, tiles, p->num_splits, &cost_w);
+  plan->wide = force_wide ? 1 : force_paired ? 0 : (cost_w < cost_p ? 1 : 0);
+  plan->splits = plan->wide ? sw : sp;
   plan->mode = plan->splits > 1 ? kReduceGlobal : kReduceNone;
   size_t ws = kWorkspaceHeader;
   if (plan->mode != kReduceNone) {
@@ -1009,17 +1040,28 @@ sv_status launch(const sv_attn_params* p, const Plan& plan, cudaStream_t stream)
   const float scale = (p->sm_scale > 0.f) ? p->sm_scale : 1.0f / sqrtf(static_cast<float>(D));
   kp.scale_log2 = scale * 1.4426950408889634f;
 
-  cudaLaunchConfig_t cfg;
-  cudaLaunchAttribute attrs[2];
-  launch_config<D>(&cfg, attrs, dim3(plan.splits, p->num_kv_heads * plan.row_tiles, p->batch), plan.paired != 0,
-                   stream);
-  if (cudaLaunchKernelEx(&cfg, tree_attention_kernel<D>, tm_kc, tm_vc, tm_tk, tm_tv, kp) != cudaSuccess)
-    return SV_ERR_CUDA;
+  if (plan.wide) {
+    const WideLaunch w{plan.splits, kp.part_o, kp.part_lse, kp.err, kp.trace, kp.trace_ctas};
+    const sv_status ws = launch_wide_attention(p, w, stream);
+    if (ws != SV_OK) return ws;
+  } else {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attrs[2];
+    launch_config<D>(&cfg, attrs, dim3(plan.splits, p->num_kv_heads * plan.row_tiles, p->batch),
+                     plan.paired != 0, stream);
+    if (cudaLaunchKernelEx(&cfg, tree_attention_kernel<D>, tm_kc, tm_vc, tm_tk, tm_tv, kp) != cudaSuccess)
+      return SV_ERR_CUDA;
+  }
   if (plan.mode == kReduceGlobal) {
     cudaLaunchConfig_t ccfg = cudaLaunchConfig_t{};
     ccfg.gridDim = dim3(static_cast<unsigned>((rows * 32 + 255) / 256), 1, 1);
     ccfg.blockDim = dim3(256, 1, 1);
     ccfg.stream = stream;
+    cudaLaunchAttribute cattr[1];
+    cattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    cattr[0].val.programmaticStreamSerializationAllowed = 1;
+    ccfg.attrs = cattr;
+    ccfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&ccfg, split_combine_kernel<D>, static_cast<const __nv_bfloat16*>(kp.part_o),
                            static_cast<const float*>(kp.part_lse), kp.out, p->lse, static_cast<int>(rows),
                            plan.splits) != cudaSuccess)
@@ -1055,13 +1097,14 @@ sv_status sv_set_trace_buffer(void* buffer, size_t bytes) {
   return SV_OK;
 }
 
-sv_status sv_tree_attention_plan(const sv_attn_params* params, int* num_splits, int* split_reduce) {
+sv_status sv_tree_attention_plan(const sv_attn_params* params, int* num_splits, int* split_reduce, int* kernel) {
   if (num_splits == nullptr || split_reduce == nullptr) return SV_ERR_INVALID_ARG;
   sv::attn::Plan plan;
   const sv_status st = sv::attn::make_plan(params, &plan);
   if (st != SV_OK) return st;
   *num_splits = plan.splits;
   *split_reduce = plan.mode;
+  if (kernel != nullptr) *kernel = plan.wide;
   return SV_OK;
 }
 

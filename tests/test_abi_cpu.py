@@ -72,7 +72,8 @@ def _fake_params(**over):
     (dict(kv_pages=1 << 20), 1),                     # list without prefix sums
     (dict(batch=0), 1),
     (dict(split_reduce=1), 1),                       # only 0 (auto) and 2 (partials) exist
-    (dict(flags=2), 1),                              # unknown option bit
+    (dict(flags=8), 1),                              # unknown option bit
+    (dict(flags=6), 1),                              # both kernels forced
 ])
 def test_attention_host_validation(lib, over, status):
     p = _fake_params(**over)

@@ -54,28 +54,37 @@ def _check(case, partial=False, num_splits=0, seqs=None, kv_heads=None, sm_scale
     return out
 
 
+# the library's choice, then each kernel forced
+KERNELS = [0, binding.SV_ATTN_KERNEL_PAIRED, binding.SV_ATTN_KERNEL_WIDE]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("splits,mode", [(0, 0), (1, 0), (2, 2), (5, 2), (7, 2)])
-def test_tiny(splits, mode):
+def test_tiny(splits, mode, kernel):
     # more splits than tiles leaves some splits empty
-    _check(make_case("tiny"), num_splits=splits, split_reduce=mode)
+    _check(make_case("tiny"), num_splits=splits, split_reduce=mode, flags=kernel)
 
 
 @pytest.mark.parametrize("splits,mode", [(0, 0), (1, 0), (2, 2), (3, 2), (9, 2), (10, 2), (16, 2), (19, 2),
                                          (34, 2)])
-def test_llama_eagle_layer(splits, mode):
-    # 240 rows per KV head: a CTA pair shares every K/V tile; splits merge
-    # through workspace partials and a combine kernel
-    _check(make_case("llama8b_eagle", layers=1, with_logits=False), num_splits=splits, split_reduce=mode)
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_llama_eagle_layer(splits, mode, kernel):
+    # 240 rows per KV head (a CTA pair sharing every K/V tile, or one
+    # 256-row CTA); splits merge through workspace partials and a combine
+    # kernel
+    _check(make_case("llama8b_eagle", layers=1, with_logits=False), num_splits=splits, split_reduce=mode,
+           flags=kernel)
 
 
 @pytest.mark.parametrize("splits,mode", [(0, 0), (1, 0), (3, 2), (5, 2), (33, 2)])
-def test_early_context_flag(splits, mode):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_early_context_flag(splits, mode, kernel):
     # the context pages and index arrays are read before the wait on the
     # preceding grid; results are unchanged
-    _check(make_case("llama8b_eagle", layers=1, with_logits=False), num_splits=splits, split_reduce=mode,
-           flags=binding.SV_ATTN_EARLY_CONTEXT)
+    f = binding.SV_ATTN_EARLY_CONTEXT | kernel
+    _check(make_case("llama8b_eagle", layers=1, with_logits=False), num_splits=splits, split_reduce=mode, flags=f)
     _check(make_case("tiny", batch=3, ctx=[0, 33, 200], with_logits=False, seed=5), num_splits=splits,
-           split_reduce=mode, flags=binding.SV_ATTN_EARLY_CONTEXT)
+           split_reduce=mode, flags=f)
 
 
 def test_early_context_back_to_back_layers():
@@ -110,33 +119,38 @@ def test_early_context_back_to_back_layers():
         assert diff <= ATOL_ATTN, (li, diff)
 
 
-def test_serving_mix_full_batch():
-    _check(make_case("serving_mix", with_logits=False))
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_serving_mix_full_batch(kernel):
+    _check(make_case("serving_mix", with_logits=False), flags=kernel)
 
 
-def test_long_context_partial_and_full():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_long_context_partial_and_full(kernel):
     case = make_case("long_partial", with_logits=False)
-    _check(case, partial=True)
-    _check(case, partial=True, num_splits=12, split_reduce=2)
-    _check(case, partial=False, kv_heads=[0, 5])
-    _check(case, partial=False, kv_heads=[3], num_splits=16, split_reduce=2)
+    _check(case, partial=True, flags=kernel)
+    _check(case, partial=True, num_splits=12, split_reduce=2, flags=kernel)
+    _check(case, partial=False, kv_heads=[0, 5], flags=kernel)
+    _check(case, partial=False, kv_heads=[3], num_splits=16, split_reduce=2, flags=kernel)
 
 
-def test_specblock_sampled():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_specblock_sampled(kernel):
     case = make_case("specblock", with_logits=False)
-    _check(case, seqs=[0, 7, 15], kv_heads=[2, 6])
+    _check(case, seqs=[0, 7, 15], kv_heads=[2, 6], flags=kernel)
 
 
-def test_specblock_full_oracle_at_short_context():
-    _check(make_case("specblock", ctx=300, with_logits=False))
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_specblock_full_oracle_at_short_context(kernel):
+    _check(make_case("specblock", ctx=300, with_logits=False), flags=kernel)
 
 
 @pytest.mark.parametrize("ctx", [[0], [1], [15], [17], [127], [129], [1000], [0, 33, 16, 200]])
-def test_ragged_and_empty_contexts(ctx):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_ragged_and_empty_contexts(ctx, kernel):
     case = make_case("tiny", batch=len(ctx), ctx=ctx, seed=sum(ctx) + 7, with_logits=False)
-    _check(case, num_splits=0)
-    _check(case, num_splits=3)
-    _check(case, num_splits=3, split_reduce=2)
+    _check(case, num_splits=0, flags=kernel)
+    _check(case, num_splits=3, flags=kernel)
+    _check(case, num_splits=3, split_reduce=2, flags=kernel)
 
 
 def test_root_only_tree_is_decode_attention():
@@ -145,10 +159,11 @@ def test_root_only_tree_is_decode_attention():
 
 
 @pytest.mark.parametrize("hq,hkv,d", [(8, 8, 128), (8, 4, 64), (16, 8, 128), (64, 8, 128), (32, 2, 64)])
-def test_group_sizes_and_head_dims(hq, hkv, d):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_group_sizes_and_head_dims(hq, hkv, d, kernel):
     case = make_case("serving_mix", batch=3, ctx=(40, 300), num_q_heads=hq, num_kv_heads=hkv, head_dim=d,
                      with_logits=False, seed=hq * 100 + hkv)
-    _check(case)
+    _check(case, flags=kernel)
 
 
 def test_chain_of_128_nodes():
@@ -157,22 +172,24 @@ def test_chain_of_128_nodes():
     _check(case)
 
 
-def test_128_nodes_at_group_8_spans_four_row_groups():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_128_nodes_at_group_8_spans_four_row_groups(kernel):
     rng = np.random.default_rng(3)
     par = [-1] + [int(rng.integers(0, i)) for i in range(1, 128)]
     case = make_case("specblock", batch=2, ctx=[100, 40], parents_list=[par, par[:77]], with_logits=False)
-    _check(case)
-    _check(case, num_splits=4)
-    _check(case, num_splits=4, split_reduce=2)
+    _check(case, flags=kernel)
+    _check(case, num_splits=4, flags=kernel)
+    _check(case, num_splits=4, split_reduce=2, flags=kernel)
 
 
 @pytest.mark.parametrize("splits", [0, 2])
-def test_partial_lists_small_settings(splits):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_partial_lists_small_settings(splits, kernel):
     # SpecPV Appendix D settings: 16-token blocks, 32 sink tokens, a 128-token
     # window plus a 20-token buffer (folded into the recent window).
     case = make_case("serving_mix", batch=4, ctx=(300, 900), with_logits=False,
                      partial=dict(sink=32, blocks=6, block_tokens=16, recent=148))
-    _check(case, partial=True, num_splits=splits)
+    _check(case, partial=True, num_splits=splits, flags=kernel)
 
 
 def test_partial_all_pages_equals_full_and_empty_list():
@@ -217,7 +234,8 @@ def test_bad_page_is_reported_not_trapped():
 
 @pytest.mark.parametrize("nodes", [1, 2, 32])
 @pytest.mark.parametrize("splits", [0, 1, 4])
-def test_pair_with_an_empty_row_tile(nodes, splits):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_pair_with_an_empty_row_tile(nodes, splits, kernel):
     # the 60-node tree needs two 128-row tiles (a CTA pair sharing each K/V
     # tile); the small tree of the other sequence leaves the second CTA of
     # its pair without rows, and that CTA must still load and release its
@@ -228,4 +246,4 @@ def test_pair_with_an_empty_row_tile(nodes, splits):
     case = make_case("llama8b_eagle", layers=1, batch=2, ctx=[777, 300], parents_list=[big, small],
                      with_logits=False, seed=nodes + 11)
     for _ in range(2):
-        _check(case, num_splits=splits, split_reduce=2 if splits > 1 else 0)
+        _check(case, num_splits=splits, split_reduce=2 if splits > 1 else 0, flags=kernel)
