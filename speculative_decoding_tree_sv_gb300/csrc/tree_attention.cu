@@ -707,17 +707,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Merge split partials: O = sum_s w_s O_s / sum_s w_s, w_s = 2^(lse_s - max).
-// One warp per output row: lane s holds split s's (and s + 32's) log2-sum-exp,
-// the weights come from warp reductions, and the partial rows are read eight
-// splits at a time so their loads overlap.  It is launched as a programmatic
-// dependent of the attention grid (whose CTAs signal once their partials are
-// written) and lets the next grid in the stream launch early in turn.
+// One warp per output row.  The log2-sum-exps (lane s holds split s and
+// s + 32) and the partial rows of up to 16 splits are all requested before
+// any is used, so a row costs one round trip to L2 per 16 splits; empty
+// splits (weight 0) may hold stale rows, so they are excluded by selection,
+// never by multiplication.  It is launched as a programmatic dependent of the
+// attention grid (whose CTAs signal once their partials are written) and lets
+// the next grid in the stream launch early in turn.
 template <int D>
 __global__ void __launch_bounds__(256) split_combine_kernel(const __nv_bfloat16* __restrict__ part_o,
                                                             const float* __restrict__ part_lse,
                                                             __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
                                                             int rows, int splits) {
   constexpr int E = D / 32;  // elements per lane
+  constexpr int kChunk = 16;
   griddep_launch_dependents();
   griddep_wait();
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -725,29 +728,18 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const __nv_bfloat16*
   if (row >= rows) return;
   const float l0 = (lane < splits) ? __ldcg(part_lse + static_cast<size_t>(lane) * rows + row) : -INFINITY;
   const float l1 = (lane + 32 < splits) ? __ldcg(part_lse + static_cast<size_t>(lane + 32) * rows + row) : -INFINITY;
-  float mx = fmaxf(l0, l1);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  const float w0 = (l0 == -INFINITY) ? 0.f : ex2(l0 - mx);
-  const float w1 = (l1 == -INFINITY) ? 0.f : ex2(l1 - mx);
-  float wsum = w0 + w1;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  for (int s0 = 0; s0 < splits; s0 += 8) {
-    float ws[8];
-    uint32_t v[8][E / 2];
+  float mx = -INFINITY, w0 = 0.f, w1 = 0.f, wsum = 0.f;
+  for (int s0 = 0; s0 < splits; s0 += kChunk) {
+    uint32_t v[kChunk][E / 2];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int s = s0 + k;
-      ws[k] = __shfl_sync(0xffffffffu, (s < 32) ? w0 : w1, s & 31);
+    for (int k = 0; k < kChunk; ++k) {
 #pragma unroll
       for (int e = 0; e < E / 2; ++e) v[k][e] = 0u;
-      // empty splits (weight 0) may hold stale rows: never read them
-      if (s < splits && ws[k] != 0.f) {
-        const __nv_bfloat16* src = part_o + (static_cast<size_t>(s) * rows + row) * D + lane * E;
+      if (s0 + k < splits) {
+        const __nv_bfloat16* src = part_o + (static_cast<size_t>(s0 + k) * rows + row) * D + lane * E;
         if constexpr (E == 4) {
           const uint2 t = __ldcg(reinterpret_cast<const uint2*>(src));
           v[k][0] = t.x;
@@ -757,13 +749,28 @@ __global__ void __launch_bounds__(256) split_combine_kernel(const __nv_bfloat16*
         }
       }
     }
+    if (s0 == 0) {  // the weights, while the first partial rows are in flight
+      mx = fmaxf(l0, l1);
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      w0 = (l0 == -INFINITY) ? 0.f : ex2(l0 - mx);
+      w1 = (l1 == -INFINITY) ? 0.f : ex2(l1 - mx);
+      wsum = w0 + w1;
 #pragma unroll
-      for (int e = 0; e < E / 2; ++e) {
-        acc[2 * e] += ws[k] * __uint_as_float(v[k][e] << 16);
-        acc[2 * e + 1] += ws[k] * __uint_as_float(v[k][e] & 0xFFFF0000u);
+      for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    }
+#pragma unroll
+    for (int k = 0; k < kChunk; ++k) {
+      const int s = s0 + k;
+      const float ws = __shfl_sync(0xffffffffu, (s < 32) ? w0 : w1, s & 31);
+      if (s < splits && ws != 0.f) {
+#pragma unroll
+        for (int e = 0; e < E / 2; ++e) {
+          acc[2 * e] += ws * __uint_as_float(v[k][e] << 16);
+          acc[2 * e + 1] += ws * __uint_as_float(v[k][e] & 0xFFFF0000u);
+        }
       }
+    }
   }
   const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
   __nv_bfloat16* dst = out + static_cast<size_t>(row) * D + lane * E;
