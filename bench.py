@@ -89,16 +89,18 @@ def measured_traffic(config: str):
     when the kernel source changed since those counters were taken."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    src = os.path.join(ROOT, "speculative_decoding_tree_sv_gb300", "csrc", "tree_attention.cu")
+    csrc = os.path.join(ROOT, "speculative_decoding_tree_sv_gb300", "csrc")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f).get(config)
     if not rec:
         return None
-    with open(src, "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()[:16]
-    return rec["dram_bytes_per_launch"] if h == rec.get("kernel_source_sha256_16") else None
+    h = hashlib.sha256()
+    for name in ("tree_attention.cu", "tree_attention_wide.cu"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return rec["dram_bytes_per_launch"] if h.hexdigest()[:16] == rec.get("kernel_source_sha256_16") else None
 
 
 class ClockSampler:

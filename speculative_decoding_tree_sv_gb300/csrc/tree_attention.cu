@@ -97,8 +97,6 @@ struct Params {
   const int* kv_pages;
   const int* cu_kv_pages;
   const __nv_bfloat16* q;
-  const __nv_bfloat16* k_cache;  // for L2 prefetch of whole (page, head) blocks
-  const __nv_bfloat16* v_cache;
   __nv_bfloat16* out;
   float* lse;
   __nv_bfloat16* part_o;  // split partials O / l (bf16), [splits][T * Hq][D]
@@ -107,7 +105,6 @@ struct Params {
   unsigned long long* trace;  // optional per-CTA phase timestamps
   long long trace_ctas;
   int num_q_heads;
-  int num_kv_heads;
   int group;  // G
   int num_pages;
   int max_pages_per_seq;
@@ -277,12 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------------ page ids
       // Resolves each context tile's eight page ids (partial list, then block
       // table, both range-checked) into the id ring, up to kIdSlots tiles
-      // ahead of the loaders, and asks L2 for the K and V of the pages this
-      // CTA will request: the loads that follow then wait for L2, not DRAM,
-      // which keeps the stage rings short of their latency bound.
-      const int lane_lo = paired ? 4 * static_cast<int>(rank) : 0;
-      const int lane_hi = paired ? lane_lo + 4 : kPagesPerTile;
-      constexpr uint32_t kPageBytes = 16 * D * 2;
+      // ahead of the loaders.
       bool ok = true;
       for (int it = 0; it < ntiles; ++it) {
         const int j = jb + it;
@@ -304,11 +296,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             phys = 0;
           }
           ids[sl * kPagesPerTile + lane] = phys;
-          if (lane >= lane_lo && lane < lane_hi) {
-            const size_t off = (static_cast<size_t>(phys) * p.num_kv_heads + kh) * (kPageBytes / 2);
-            l2_prefetch_bulk(p.k_cache + off, kPageBytes);
-            l2_prefetch_bulk(p.v_cache + off, kPageBytes);
-          }
         }
         __syncwarp();
         if (lane == 0) {
@@ -1014,9 +1001,6 @@ sv_status launch(const sv_attn_params* p, const Plan& plan, cudaStream_t stream)
   kp.kv_pages = p->kv_pages;
   kp.cu_kv_pages = p->cu_kv_pages;
   kp.q = static_cast<const __nv_bfloat16*>(p->q);
-  kp.k_cache = static_cast<const __nv_bfloat16*>(p->k_cache);
-  kp.v_cache = static_cast<const __nv_bfloat16*>(p->v_cache);
-  kp.num_kv_heads = p->num_kv_heads;
   kp.out = static_cast<__nv_bfloat16*>(p->out);
   kp.lse = p->lse;
   kp.err = reinterpret_cast<int*>(ws);
