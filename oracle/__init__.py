@@ -10,6 +10,8 @@ verification hot path computes, written from the method descriptions:
   root path and its bonus token.
 * ``commit``     — the KV cache after the accepted path is written to slots
   L .. L + a.
+* ``retrieval``  — SpecPV block retrieval: max/min key summaries of 16-token
+  pages, block importance against the tree's queries, the partial page list.
 
 Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU
 baseline leg may import this package.  The CUDA library never calls it and
@@ -29,3 +31,10 @@ from .attention import (  # noqa: F401
 )
 from .accept import greedy_accept  # noqa: F401
 from .commit import kv_commit  # noqa: F401
+from .retrieval import (  # noqa: F401
+    block_importance,
+    page_regions,
+    page_summaries,
+    query_block_score,
+    retrieve_pages,
+)

@@ -1,0 +1,141 @@
+"""Oracle for SpecPV block retrieval (float64) — TEST INFRASTRUCTURE ONLY.
+
+What is computed, from SpecPV:
+
+* section 3.2 "Partial Verification": the partial KV cache keeps the initial
+  sink blocks, query-dependent retrieved blocks, a fixed-size local window
+  and a buffer, attended as one continuous segment; key-state summaries of
+  every block are cached to speed up retrieval, and they are the
+  element-wise maximum and minimum of the block's key states; blocks are
+  scored against several candidate tokens' query states and the per-query
+  scores are reduced to one block-importance score by a reduction such as
+  max, mean or last;
+* Appendix C: mean reduction works best;  Appendix D: blocks of 16 tokens.
+
+Readings where the pages are silent (also listed in the design notes):
+
+* The score of a block for one query q (query head h, KV head h // G) is the
+  largest value q . k can take for a key k lying element-wise between the
+  block's minimum and maximum key: sum_d max(q_d * kmax_d, q_d * kmin_d).  It
+  bounds q . k from above for every key of the block.
+* A block's importance reduces those scores over all candidate tokens (the
+  tree's nodes) and all query heads: their mean ("mean"), their maximum
+  ("max"), or the mean over query heads for the last node in index order
+  ("last").
+* A block is one 16-token page (logical page p holds tokens 16p .. 16p+15;
+  the last page of a context may be partial and its summary covers only its
+  valid tokens).
+* Sink pages are the first ceil(sink_tokens / 16) pages; window pages are
+  those holding the last window_tokens tokens.  The other pages are the
+  candidates; the topk most important (ties: lower page id first) are
+  retrieved.  The partial list is sink, retrieved and window pages in
+  ascending order.  (SpecPV's buffer of partially verified tokens lies at
+  the end of the context and is covered by the window.)
+
+Only the test suite may import this module.
+"""
+
+from __future__ import annotations
+
+from typing import Dict, List, Optional, Sequence, Tuple
+
+import numpy as np
+
+from .attention import bf16_to_f64
+
+REDUCTIONS = ("mean", "max", "last")
+
+
+def page_summaries(k_cache: np.ndarray, block_table: np.ndarray, ctx_lens: Sequence[int],
+                   page_size: int = 16) -> Tuple[np.ndarray, np.ndarray]:
+    """Element-wise max and min of the valid keys of every page in use.
+
+    k_cache: bf16 bits [num_pages, Hkv, page_size, D].  Returns
+    (summary float64 [num_pages, Hkv, 2, D] with [:, :, 0] = max and
+    [:, :, 1] = min, defined bool [num_pages]).  Pages no sequence uses stay
+    zero and undefined."""
+    num_pages, hkv, ps, d = k_cache.shape
+    assert ps == page_size
+    summ = np.zeros((num_pages, hkv, 2, d), dtype=np.float64)
+    defined = np.zeros(num_pages, dtype=bool)
+    for b, L in enumerate(ctx_lens):
+        L = int(L)
+        for lp in range((L + page_size - 1) // page_size):
+            phys = int(block_table[b, lp])
+            valid = min(page_size, L - lp * page_size)
+            keys = bf16_to_f64(k_cache[phys, :, :valid, :])  # [Hkv, valid, D]
+            summ[phys, :, 0, :] = keys.max(axis=1)
+            summ[phys, :, 1, :] = keys.min(axis=1)
+            defined[phys] = True
+    return summ, defined
+
+
+def query_block_score(q: np.ndarray, kmax: np.ndarray, kmin: np.ndarray) -> float:
+    """Largest q . k for any key k with kmin <= k <= kmax element-wise."""
+    return float(np.sum(np.maximum(q * kmax, q * kmin)))
+
+
+def page_regions(ctx_len: int, sink_tokens: int, window_tokens: int,
+                 page_size: int = 16) -> Tuple[int, int, int]:
+    """(n_pages, number of sink pages, first window page) of a context."""
+    n_pages = (int(ctx_len) + page_size - 1) // page_size
+    sink = min(n_pages, (int(sink_tokens) + page_size - 1) // page_size)
+    first_window = min(n_pages, max(0, int(ctx_len) - int(window_tokens)) // page_size)
+    first_window = max(first_window, sink)
+    return n_pages, sink, first_window
+
+
+def block_importance(q_seq: np.ndarray, summ: np.ndarray, phys_pages: Sequence[int], num_kv_heads: int,
+                     reduce: str) -> np.ndarray:
+    """Importance of each listed physical page for one sequence.
+
+    q_seq: query values float64 [N, Hq, D] (post-RoPE) of the sequence's tree
+    nodes; summ as returned by page_summaries."""
+    n, hq, _ = q_seq.shape
+    g = hq // num_kv_heads
+    out = np.zeros(len(phys_pages), dtype=np.float64)
+    nodes = [n - 1] if reduce == "last" else list(range(n))
+    for pi, phys in enumerate(phys_pages):
+        scores = []
+        for i in nodes:
+            for h in range(hq):
+                kv = h // g
+                scores.append(query_block_score(q_seq[i, h], summ[phys, kv, 0], summ[phys, kv, 1]))
+        if reduce == "max":
+            out[pi] = max(scores)
+        elif reduce in ("mean", "last"):
+            out[pi] = float(np.mean(scores))
+        else:
+            raise ValueError(reduce)
+    return out
+
+
+def retrieve_pages(q: np.ndarray, k_cache: np.ndarray, block_table: np.ndarray, ctx_lens: Sequence[int],
+                   cu_nodes: Sequence[int], sink_tokens: int, window_tokens: int, topk: int,
+                   reduce: str = "mean", page_size: int = 16
+                   ) -> Tuple[np.ndarray, np.ndarray, List[Dict[int, float]]]:
+    """Partial page lists of every sequence.
+
+    q: bf16 bits [T, Hq, D].  Returns (kv_pages int32, cu_kv_pages int32
+    [B+1], per sequence a dict logical candidate page -> importance)."""
+    if reduce not in REDUCTIONS:
+        raise ValueError(reduce)
+    num_kv_heads = k_cache.shape[1]
+    summ, _ = page_summaries(k_cache, block_table, ctx_lens, page_size)
+    qf = bf16_to_f64(q)
+    lists, scores_all = [], []
+    for b, L in enumerate(ctx_lens):
+        n_pages, sink, first_window = page_regions(int(L), sink_tokens, window_tokens, page_size)
+        cand = list(range(sink, first_window))
+        imp = block_importance(qf[cu_nodes[b]:cu_nodes[b + 1]], summ, [int(block_table[b, p]) for p in cand],
+                               num_kv_heads, reduce)
+        scores_all.append({p: float(s) for p, s in zip(cand, imp)})
+        order = sorted(range(len(cand)), key=lambda i: (-imp[i], cand[i]))
+        chosen = {cand[i] for i in order[:min(int(topk), len(cand))]}
+        keep = set(range(sink)) | chosen | set(range(first_window, n_pages))
+        lists.append(sorted(keep))
+    cu = np.zeros(len(lists) + 1, dtype=np.int32)
+    for b, lst in enumerate(lists):
+        cu[b + 1] = cu[b] + len(lst)
+    flat = np.array([p for lst in lists for p in lst], dtype=np.int32)
+    return flat, cu, scores_all
