@@ -265,6 +265,81 @@ sv_status sv_kv_commit(const void* tree_k, const void* tree_v, long long tree_la
                        int* new_ctx_lens, void* workspace, size_t workspace_bytes,
                        sv_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * SpecPV block retrieval: the partial page list of sv_tree_attention.
+ *
+ * Defined by: SpecPV section 3.2 (the partial KV cache keeps sink blocks,
+ * query-dependent retrieved blocks and a local window, attended as one
+ * segment; every block's keys are summarised by their element-wise maximum
+ * and minimum; blocks are scored against the candidate tokens' query states
+ * and the per-query scores reduced by max, mean or last), Appendix C (mean
+ * works best) and Appendix D (16-token blocks).
+ *
+ * A block is one 16-token page.  The score of page p for query q (query
+ * head h, KV head h / G) is the largest q . k for a key between the page's
+ * minimum and maximum key, sum_d max(q_d kmax_d, q_d kmin_d).  A page's
+ * importance is the mean of its scores over every tree node and query head
+ * of the sequence (SV_REDUCE_MEAN), their maximum (SV_REDUCE_MAX), or the
+ * mean over query heads for the last node in index order (SV_REDUCE_LAST).
+ * Sink pages are the first ceil(sink_tokens / 16); window pages hold the
+ * last window_tokens tokens; of the pages in between the topk most important
+ * are retrieved (equal importance: lower page first).  The list of a
+ * sequence is its sink, retrieved and window pages, ascending: exactly the
+ * kv_pages / cu_kv_pages input of sv_tree_attention (max_kv_pages <=
+ * ceil(sink/16) + topk + ceil(window/16) + 1).
+ * ---------------------------------------------------------------------- */
+
+/* Page summaries: for every page of every sequence from logical page
+ * first_page[b] on (first_page NULL: all), the element-wise maximum and
+ * minimum of the page's valid keys (tokens below ctx_lens[b]), per KV head.
+ * After sv_kv_commit, passing first_page = old ctx_lens / 16 and the new
+ * lengths refreshes exactly the pages the commit touched.
+ *   k_cache     bf16 [num_pages, Hkv, page_size, D] (one layer)
+ *   summaries   bf16 [num_pages, Hkv, 2, D]: [.., 0, :] maximum, [.., 1, :]
+ *               minimum; pages no sequence uses are left untouched
+ *   max_ctx_pages (host) >= every ceil(ctx_lens[b] / 16) - first_page[b]
+ *   workspace   optional (NULL, or >= 256 bytes zero-filled once): error word */
+sv_status sv_kv_page_summaries(const void* k_cache, int num_pages, int num_kv_heads, int head_dim, int page_size,
+                               const int* block_table, int max_pages_per_seq, const int* ctx_lens,
+                               const int* first_page, int batch, int max_ctx_pages, void* summaries,
+                               void* workspace, size_t workspace_bytes, sv_stream_t stream);
+
+typedef enum sv_reduce { SV_REDUCE_MEAN = 0, SV_REDUCE_MAX = 1, SV_REDUCE_LAST = 2 } sv_reduce;
+
+typedef struct sv_retrieve_params {
+  int batch;              /* B                                              */
+  int num_q_heads;        /* Hq                                             */
+  int num_kv_heads;       /* Hkv                                            */
+  int head_dim;           /* D: 64 or 128                                   */
+  int page_size;          /* 16                                             */
+  int num_pages;          /* pages in the pool                              */
+  int total_nodes;        /* T = cu_nodes[B]                                */
+  int max_pages_per_seq;  /* row length of block_table                      */
+  int max_ctx_pages;      /* host: max_b ceil(ctx_lens[b] / 16), <= 16384   */
+  int sink_tokens;
+  int window_tokens;
+  int topk;               /* pages retrieved between sink and window        */
+  int reduce;             /* sv_reduce                                      */
+  const void* q;          /* bf16 [T, Hq, D] the tree nodes' queries        */
+  const void* summaries;  /* bf16 [num_pages, Hkv, 2, D] (sv_kv_page_summaries) */
+  const int* block_table; /* int32 [B, max_pages_per_seq]                   */
+  const int* ctx_lens;    /* int32 [B]                                      */
+  const int* cu_nodes;    /* int32 [B+1]                                    */
+  int* kv_pages;          /* out: int32, the lists packed in sequence order */
+  int* cu_kv_pages;       /* out: int32 [B+1] prefix sums                   */
+  float* scores;          /* optional out: fp32 [B, max_ctx_pages], the
+                             importance of every candidate page, -inf for
+                             the others                                     */
+  size_t kv_pages_capacity; /* entries of kv_pages (>= B x the list bound)  */
+  void* workspace;        /* sv_retrieve_pages_workspace_size bytes         */
+  size_t workspace_bytes;
+} sv_retrieve_params;
+
+sv_status sv_retrieve_pages_workspace_size(int batch, int num_kv_heads, int head_dim, int max_ctx_pages,
+                                           size_t* bytes);
+
+sv_status sv_retrieve_pages(const sv_retrieve_params* params, sv_stream_t stream);
+
 /* Diagnostics: per-CTA phase tracing of sv_tree_attention.
  *
  * After this call, every sv_tree_attention launch (until the buffer is

@@ -47,6 +47,20 @@ class sv_attn_params(ctypes.Structure):
     ]
 
 
+class sv_retrieve_params(ctypes.Structure):
+    _fields_ = [
+        ("batch", c_int), ("num_q_heads", c_int), ("num_kv_heads", c_int), ("head_dim", c_int),
+        ("page_size", c_int), ("num_pages", c_int), ("total_nodes", c_int), ("max_pages_per_seq", c_int),
+        ("max_ctx_pages", c_int), ("sink_tokens", c_int), ("window_tokens", c_int), ("topk", c_int),
+        ("reduce", c_int),
+        ("q", c_void_p), ("summaries", c_void_p), ("block_table", c_void_p), ("ctx_lens", c_void_p),
+        ("cu_nodes", c_void_p), ("kv_pages", c_void_p), ("cu_kv_pages", c_void_p), ("scores", c_void_p),
+        ("kv_pages_capacity", c_size_t), ("workspace", c_void_p), ("workspace_bytes", c_size_t),
+    ]
+
+
+SV_REDUCE_MEAN, SV_REDUCE_MAX, SV_REDUCE_LAST = 0, 1, 2
+
 _LIB = None
 
 
@@ -83,6 +97,13 @@ def load(path: Optional[str] = None):
     lib.sv_kv_commit.argtypes = [c_void_p, c_void_p, c_longlong, c_void_p, c_void_p, c_longlong, c_int, c_int,
                                  c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                                  c_int, c_int, c_void_p, c_void_p, c_size_t, c_void_p]
+    lib.sv_kv_page_summaries.restype = c_int
+    lib.sv_kv_page_summaries.argtypes = [c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_int, c_void_p, c_void_p,
+                                         c_int, c_int, c_void_p, c_void_p, c_size_t, c_void_p]
+    lib.sv_retrieve_pages_workspace_size.restype = c_int
+    lib.sv_retrieve_pages_workspace_size.argtypes = [c_int, c_int, c_int, c_int, P(c_size_t)]
+    lib.sv_retrieve_pages.restype = c_int
+    lib.sv_retrieve_pages.argtypes = [P(sv_retrieve_params), c_void_p]
     lib.sv_set_trace_buffer.restype = c_int
     lib.sv_set_trace_buffer.argtypes = [c_void_p, c_size_t]
     lib.sv_get_device_error.restype = c_int
@@ -220,6 +241,55 @@ def sv_kv_commit(tree_k, tree_v, tree_layer_stride: int, k_cache, v_cache, cache
                                _ptr(ctx_lens), _ptr(cu_nodes), _ptr(accepted_nodes), _ptr(accept_len), batch,
                                max_depth, num_kv_heads, head_dim, page_size, _ptr(new_ctx_lens),
                                _ptr(workspace), workspace_bytes, _stream(stream)), "sv_kv_commit")
+
+
+def sv_kv_page_summaries(k_cache, num_pages: int, num_kv_heads: int, head_dim: int, block_table,
+                         max_pages_per_seq: int, ctx_lens, first_page, batch: int, max_ctx_pages: int, summaries,
+                         workspace=None, workspace_bytes: int = 0, page_size: int = 16, stream=None) -> None:
+    if workspace is not None and not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(load().sv_kv_page_summaries(_ptr(k_cache), num_pages, num_kv_heads, head_dim, page_size,
+                                       _ptr(block_table), max_pages_per_seq, _ptr(ctx_lens), _ptr(first_page),
+                                       batch, max_ctx_pages, _ptr(summaries), _ptr(workspace), workspace_bytes,
+                                       _stream(stream)), "sv_kv_page_summaries")
+
+
+def retrieve_list_bound(sink_tokens: int, window_tokens: int, topk: int, page_size: int = 16) -> int:
+    """Longest partial list sv_retrieve_pages writes for one sequence."""
+    return -(-sink_tokens // page_size) + topk + -(-window_tokens // page_size) + 1
+
+
+def sv_retrieve_pages_workspace_size(batch: int, num_kv_heads: int, head_dim: int, max_ctx_pages: int) -> int:
+    n = c_size_t(0)
+    _check(load().sv_retrieve_pages_workspace_size(batch, num_kv_heads, head_dim, max_ctx_pages, ctypes.byref(n)),
+           "sv_retrieve_pages_workspace_size")
+    return int(n.value)
+
+
+def make_retrieve_params(*, q, summaries, block_table, ctx_lens, cu_nodes, kv_pages, cu_kv_pages, batch: int,
+                         num_q_heads: int, num_kv_heads: int, head_dim: int, num_pages: int, total_nodes: int,
+                         max_pages_per_seq: int, max_ctx_pages: int, sink_tokens: int, window_tokens: int,
+                         topk: int, reduce: int = SV_REDUCE_MEAN, scores=None, kv_pages_capacity=None,
+                         workspace=None, workspace_bytes: int = 0, page_size: int = 16) -> sv_retrieve_params:
+    r = sv_retrieve_params()
+    r.batch, r.num_q_heads, r.num_kv_heads, r.head_dim = batch, num_q_heads, num_kv_heads, head_dim
+    r.page_size, r.num_pages, r.total_nodes, r.max_pages_per_seq = page_size, num_pages, total_nodes, max_pages_per_seq
+    r.max_ctx_pages, r.sink_tokens, r.window_tokens, r.topk, r.reduce = (max_ctx_pages, sink_tokens, window_tokens,
+                                                                         topk, reduce)
+    r.q, r.summaries, r.block_table, r.ctx_lens, r.cu_nodes = (_ptr(q), _ptr(summaries), _ptr(block_table),
+                                                              _ptr(ctx_lens), _ptr(cu_nodes))
+    r.kv_pages, r.cu_kv_pages, r.scores = _ptr(kv_pages), _ptr(cu_kv_pages), _ptr(scores)
+    if kv_pages_capacity is None:
+        kv_pages_capacity = kv_pages.numel() if hasattr(kv_pages, "numel") else 0
+    r.kv_pages_capacity = int(kv_pages_capacity)
+    r.workspace = _ptr(workspace)
+    r.workspace_bytes = int(workspace_bytes if workspace_bytes else
+                            (workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0))
+    return r
+
+
+def sv_retrieve_pages(params: sv_retrieve_params, stream=None) -> None:
+    _check(load().sv_retrieve_pages(ctypes.byref(params), _stream(stream)), "sv_retrieve_pages")
 
 
 TRACE_SLOTS = 16

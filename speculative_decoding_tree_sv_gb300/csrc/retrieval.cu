@@ -1,0 +1,531 @@
+// SpecPV block retrieval for sm_103a.
+//
+// SpecPV section 3.2 "Partial Verification": the partial KV cache keeps the
+// initial sink blocks, query-dependent retrieved blocks and a local window
+// (with the buffer of partially verified tokens at its end), attended as one
+// segment; every block's keys are summarised by their element-wise maximum
+// and minimum, cached, and scored against the candidate tokens' query states;
+// the per-query scores are reduced to one importance per block (max, mean or
+// last; Appendix C: mean works best).  Blocks are 16-token pages (Appendix D).
+//
+// Score of a block for one query q: the largest q . k over keys between the
+// block's minimum and maximum, sum_d max(q_d kmax_d, q_d kmin_d)
+// = q+ . kmax + q- . kmin with q+ = max(q, 0), q- = min(q, 0).  That form is
+// linear in (q+, q-), so the mean over queries (and the mean over heads of the
+// last node) is the dot product of the averaged (q+, q-) with the summary: a
+// GEMV over the summaries, bound by reading them.  The max reduction needs
+// every query's score and runs one query row at a time.
+//
+// Kernels: page_summary_kernel (one warp per (page, KV head): max/min of the
+// page's valid keys, bf16), query_aggregate_kernel (averaged q+, q- per
+// (sequence, KV head)), page_score_kernel (one warp per page),
+// select_kernel (one CTA per sequence: bitonic sort of the candidates'
+// (score, page) keys in shared memory, top-k, then the sink, retrieved and
+// window pages written in ascending order).
+#include <math.h>
+
+#include <algorithm>
+
+#include "sv_device.cuh"
+
+namespace sv {
+namespace retr {
+
+constexpr int kPage = 16;
+constexpr int kMaxSortPages = 16384;  // candidate pages per sequence sorted in shared memory
+constexpr int kSelThreads = 1024;
+constexpr int kWarpsPerCta = 8;
+
+// Sink pages, first window page and page count of a context (the same
+// regions for every kernel).  Contexts longer than max_ctx_pages pages (a
+// host value that should bound them) are cut to that many pages.
+struct Regions {
+  int n_pages, sink, first_window;
+};
+
+__device__ __forceinline__ int clamp_len(int L, int max_ctx_pages) { return min(L, max_ctx_pages * kPage); }
+
+__device__ __forceinline__ Regions regions(int L, int sink_tokens, int window_tokens) {
+  Regions r;
+  r.n_pages = (L + kPage - 1) / kPage;
+  r.sink = min(r.n_pages, (sink_tokens + kPage - 1) / kPage);
+  r.first_window = max(r.sink, min(r.n_pages, max(0, L - window_tokens) / kPage));
+  return r;
+}
+
+__device__ __forceinline__ int list_length(int L, int sink_tokens, int window_tokens, int topk) {
+  const Regions r = regions(L, sink_tokens, window_tokens);
+  return r.sink + min(topk, r.first_window - r.sink) + (r.n_pages - r.first_window);
+}
+
+// ------------------------------------------------------------------ summaries
+
+struct SumParams {
+  const __nv_bfloat16* k_cache;  // [num_pages, Hkv, 16, D]
+  __nv_bfloat16* summ;           // [num_pages, Hkv, 2, D]: max, then min
+  const int* block_table;
+  const int* ctx_lens;
+  const int* first_page;  // optional [B]
+  int* err;
+  int num_pages;
+  int num_kv_heads;
+  int max_pages_per_seq;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) page_summary_kernel(const __grid_constant__ SumParams p) {
+  constexpr int E = D / 32;  // elements per lane
+  const int b = blockIdx.y;
+  const int w = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int L = p.ctx_lens[b];
+  const int n_pages = (L + kPage - 1) / kPage;
+  const int lp = (p.first_page != nullptr ? max(0, p.first_page[b]) : 0) + w / p.num_kv_heads;
+  const int h = w % p.num_kv_heads;
+  if (lp >= n_pages) return;
+  if (lp >= p.max_pages_per_seq) {
+    if (lane == 0) report_error(p.err, SV_DEVERR_BAD_PAGE);
+    return;
+  }
+  const int phys = p.block_table[static_cast<size_t>(b) * p.max_pages_per_seq + lp];
+  if (phys < 0 || phys >= p.num_pages) {
+    if (lane == 0) report_error(p.err, SV_DEVERR_BAD_PAGE);
+    return;
+  }
+  const int valid = min(kPage, L - lp * kPage);
+  const __nv_bfloat16* src = p.k_cache + (static_cast<size_t>(phys) * p.num_kv_heads + h) * kPage * D + lane * E;
+  float mx[E], mn[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    mx[e] = -INFINITY;
+    mn[e] = INFINITY;
+  }
+  for (int t = 0; t < valid; ++t) {
+    uint32_t v[E / 2];
+    if constexpr (E == 4) {
+      const uint2 x = __ldg(reinterpret_cast<const uint2*>(src + t * D));
+      v[0] = x.x;
+      v[1] = x.y;
+    } else {
+      v[0] = __ldg(reinterpret_cast<const unsigned int*>(src + t * D));
+    }
+#pragma unroll
+    for (int e = 0; e < E / 2; ++e) {
+      const float lo = __uint_as_float(v[e] << 16), hi = __uint_as_float(v[e] & 0xFFFF0000u);
+      mx[2 * e] = fmaxf(mx[2 * e], lo);
+      mn[2 * e] = fminf(mn[2 * e], lo);
+      mx[2 * e + 1] = fmaxf(mx[2 * e + 1], hi);
+      mn[2 * e + 1] = fminf(mn[2 * e + 1], hi);
+    }
+  }
+  // max and min of bf16 values are bf16 values: the conversion back is exact
+  __nv_bfloat16* dst = p.summ + (static_cast<size_t>(phys) * p.num_kv_heads + h) * 2 * D + lane * E;
+  uint32_t omx[E / 2], omn[E / 2];
+#pragma unroll
+  for (int e = 0; e < E / 2; ++e) {
+    omx[e] = pack_bf16x2(mx[2 * e], mx[2 * e + 1]);
+    omn[e] = pack_bf16x2(mn[2 * e], mn[2 * e + 1]);
+  }
+  if constexpr (E == 4) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(omx[0], omx[1]);
+    *reinterpret_cast<uint2*>(dst + D) = make_uint2(omn[0], omn[1]);
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = omx[0];
+    *reinterpret_cast<uint32_t*>(dst + D) = omn[0];
+  }
+}
+
+// ------------------------------------------------------------------ queries
+
+struct AggParams {
+  const __nv_bfloat16* q;  // [T, Hq, D]
+  const int* cu_nodes;
+  float* qa;               // [B, Hkv, 2, D]: averaged q+ and q-
+  int num_q_heads;
+  int group;
+  int last_only;
+};
+
+// The mean over the used queries of q+ and q-, split by KV head: the sum
+// over KV heads of qa . (kmax, kmin) is then the mean score.  One CTA per
+// (KV head, sequence), one thread per head dimension.
+template <int D>
+__global__ void __launch_bounds__(D) query_aggregate_kernel(const __grid_constant__ AggParams p) {
+  const int kvh = blockIdx.x;
+  const int b = blockIdx.y;
+  const int d = threadIdx.x;
+  const int n0 = p.cu_nodes[b];
+  const int N = p.cu_nodes[b + 1] - n0;
+  const int i0 = p.last_only ? max(0, N - 1) : 0;
+  const int used = N - i0;
+  float pos = 0.f, neg = 0.f;
+  for (int i = i0; i < N; ++i) {
+    const __nv_bfloat16* row = p.q + (static_cast<size_t>(n0 + i) * p.num_q_heads + kvh * p.group) * D + d;
+    for (int g = 0; g < p.group; ++g) {
+      const float v = __bfloat162float(row[static_cast<size_t>(g) * D]);
+      pos += fmaxf(v, 0.f);
+      neg += fminf(v, 0.f);
+    }
+  }
+  const float scale = used > 0 ? 1.f / (static_cast<float>(used) * p.num_q_heads) : 0.f;
+  float* dst = p.qa + (static_cast<size_t>(b) * gridDim.x + kvh) * 2 * D + d;
+  dst[0] = pos * scale;
+  dst[D] = neg * scale;
+}
+
+// ------------------------------------------------------------------ scores
+
+struct ScoreParams {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* summ;
+  const float* qa;
+  const int* block_table;
+  const int* ctx_lens;
+  const int* cu_nodes;
+  float* scores;  // [B, max_ctx_pages]; -inf for pages that are not candidates
+  int* err;
+  int num_pages;
+  int num_q_heads;
+  int num_kv_heads;
+  int group;
+  int max_pages_per_seq;
+  int max_ctx_pages;
+  int sink_tokens;
+  int window_tokens;
+  int reduce_max;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) page_score_kernel(const __grid_constant__ ScoreParams p) {
+  constexpr int E = D / 32;
+  const int b = blockIdx.y;
+  const int lp = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (lp >= p.max_ctx_pages) return;
+  const int L = clamp_len(p.ctx_lens[b], p.max_ctx_pages);
+  const Regions rg = regions(L, p.sink_tokens, p.window_tokens);
+  float out = -INFINITY;
+  if (lp >= rg.sink && lp < rg.first_window && lp < p.max_pages_per_seq) {
+    int phys = p.block_table[static_cast<size_t>(b) * p.max_pages_per_seq + lp];
+    if (phys < 0 || phys >= p.num_pages) {
+      if (lane == 0) report_error(p.err, SV_DEVERR_BAD_PAGE);
+      phys = 0;
+    }
+    if (!p.reduce_max) {
+      float acc = 0.f;
+      for (int kvh = 0; kvh < p.num_kv_heads; ++kvh) {
+        const __nv_bfloat16* s = p.summ + (static_cast<size_t>(phys) * p.num_kv_heads + kvh) * 2 * D + lane * E;
+        const float* a = p.qa + (static_cast<size_t>(b) * p.num_kv_heads + kvh) * 2 * D + lane * E;
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+          acc += a[e] * __bfloat162float(s[e]) + a[D + e] * __bfloat162float(s[D + e]);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      out = acc;
+    } else {
+      const int n0 = p.cu_nodes[b];
+      const int rows = (p.cu_nodes[b + 1] - n0) * p.group;
+      float best = -INFINITY;
+      for (int kvh = 0; kvh < p.num_kv_heads; ++kvh) {
+        const __nv_bfloat16* s = p.summ + (static_cast<size_t>(phys) * p.num_kv_heads + kvh) * 2 * D + lane * E;
+        float kmx[E], kmn[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          kmx[e] = __bfloat162float(s[e]);
+          kmn[e] = __bfloat162float(s[D + e]);
+        }
+        for (int r0 = 0; r0 < rows; r0 += 4) {
+          float part[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            part[u] = 0.f;
+            const int r = min(r0 + u, rows - 1);
+            const __nv_bfloat16* qr =
+                p.q + (static_cast<size_t>(n0 + r / p.group) * p.num_q_heads + kvh * p.group + r % p.group) * D +
+                lane * E;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+              const float v = __bfloat162float(qr[e]);
+              part[u] += fmaxf(v * kmx[e], v * kmn[e]);
+            }
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) part[u] += __shfl_xor_sync(0xffffffffu, part[u], o);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) best = fmaxf(best, part[u]);  // repeats of the last row are harmless
+        }
+      }
+      out = best;
+    }
+  }
+  if (lane == 0) p.scores[static_cast<size_t>(b) * p.max_ctx_pages + lp] = out;
+}
+
+// ------------------------------------------------------------------ selection
+
+struct SelParams {
+  const float* scores;
+  const int* ctx_lens;
+  int* kv_pages;
+  int* cu_kv_pages;
+  int* err;
+  int batch;
+  int max_ctx_pages;
+  int sink_tokens;
+  int window_tokens;
+  int topk;
+  int sort_len;  // power of two >= every sequence's candidate count
+};
+
+// Order-preserving map of a float to an unsigned integer.
+__device__ __forceinline__ uint32_t ordered(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_constant__ SelParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem_raw);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(keys + p.sort_len);  // [kMaxSortPages / 32]
+  int* scan = reinterpret_cast<int*>(bits + kMaxSortPages / 32);    // [kSelThreads]
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  if (tid == 0 && p.ctx_lens[b] > p.max_ctx_pages * kPage) report_error(p.err, SV_DEVERR_BAD_PAGE);
+  const int L = clamp_len(p.ctx_lens[b], p.max_ctx_pages);
+  const Regions rg = regions(L, p.sink_tokens, p.window_tokens);
+  const int ncand = rg.first_window - rg.sink;
+  const int k = min(p.topk, ncand);
+  // where this sequence's list starts: the lengths of the earlier lists
+  int part = 0;
+  for (int j = tid; j < b; j += kSelThreads)
+    part += list_length(clamp_len(p.ctx_lens[j], p.max_ctx_pages), p.sink_tokens, p.window_tokens, p.topk);
+  scan[tid] = part;
+  __syncthreads();
+  for (int s = kSelThreads / 2; s > 0; s >>= 1) {
+    if (tid < s) scan[tid] += scan[tid + s];
+    __syncthreads();
+  }
+  const int offset = scan[0];
+  __syncthreads();
+  // keys: high word the ordered score, low word the inverted page, so one
+  // descending sort ranks by score and then by lower page
+  int n2 = 1;
+  while (n2 < ncand) n2 <<= 1;
+  for (int i = tid; i < n2; i += kSelThreads) {
+    unsigned long long key = 0ull;
+    if (i < ncand) {
+      const int page = rg.sink + i;
+      const float sc = p.scores[static_cast<size_t>(b) * p.max_ctx_pages + page];
+      key = (static_cast<unsigned long long>(ordered(sc)) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(page));
+    }
+    keys[i] = key;
+  }
+  for (int i = tid; i < kMaxSortPages / 32; i += kSelThreads) bits[i] = 0u;
+  __syncthreads();
+  for (int kk = 2; kk <= n2; kk <<= 1) {
+    for (int j = kk >> 1; j > 0; j >>= 1) {
+      for (int i = tid; i < n2; i += kSelThreads) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned long long a = keys[i], c = keys[ixj];
+          const bool desc = (i & kk) == 0;
+          if (desc ? (a < c) : (a > c)) {
+            keys[i] = c;
+            keys[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // mark the retrieved, sink and window pages, then write them in order
+  for (int i = tid; i < k; i += kSelThreads) {
+    const int page = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(keys[i] & 0xFFFFFFFFull));
+    atomicOr(&bits[page >> 5], 1u << (page & 31));
+  }
+  for (int page = tid; page < rg.n_pages; page += kSelThreads)
+    if (page < rg.sink || page >= rg.first_window) atomicOr(&bits[page >> 5], 1u << (page & 31));
+  __syncthreads();
+  const int words = (rg.n_pages + 31) / 32;
+  const int per = (words + kSelThreads - 1) / kSelThreads;  // words per thread
+  const int w0 = min(words, tid * per), w1 = min(words, w0 + per);
+  int cnt = 0;
+  for (int w = w0; w < w1; ++w) cnt += __popc(bits[w]);
+  scan[tid] = cnt;
+  __syncthreads();
+  for (int s = 1; s < kSelThreads; s <<= 1) {  // inclusive scan
+    const int v = (tid >= s) ? scan[tid - s] : 0;
+    __syncthreads();
+    scan[tid] += v;
+    __syncthreads();
+  }
+  int pos = offset + scan[tid] - cnt;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t m = bits[w];
+    while (m) {
+      const int bit = __ffs(m) - 1;
+      m &= m - 1;
+      p.kv_pages[pos++] = w * 32 + bit;
+    }
+  }
+  if (tid == 0) {
+    p.cu_kv_pages[b + 1] = offset + list_length(L, p.sink_tokens, p.window_tokens, p.topk);
+    if (b == 0) p.cu_kv_pages[0] = 0;
+  }
+}
+
+size_t select_smem_bytes(int sort_len) {
+  return static_cast<size_t>(sort_len) * 8 + kMaxSortPages / 8 + kSelThreads * 4;
+}
+
+int pow2_at_least(int n) {
+  int v = 1;
+  while (v < n) v <<= 1;
+  return v;
+}
+
+}  // namespace retr
+}  // namespace sv
+
+extern "C" {
+
+sv_status sv_kv_page_summaries(const void* k_cache, int num_pages, int num_kv_heads, int head_dim, int page_size,
+                               const int* block_table, int max_pages_per_seq, const int* ctx_lens,
+                               const int* first_page, int batch, int max_ctx_pages, void* summaries,
+                               void* workspace, size_t workspace_bytes, sv_stream_t stream) {
+  using namespace sv;
+  if (!k_cache || !block_table || !ctx_lens || !summaries) return SV_ERR_INVALID_ARG;
+  if (num_pages < 1 || num_kv_heads < 1 || batch < 1 || max_pages_per_seq < 1 || max_ctx_pages < 0)
+    return SV_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return SV_ERR_UNSUPPORTED;
+  if (page_size != retr::kPage) return SV_ERR_UNSUPPORTED;
+  if (!aligned16(k_cache) || !aligned16(summaries)) return SV_ERR_INVALID_ARG;
+  if (workspace != nullptr && workspace_bytes < kWorkspaceHeader) return SV_ERR_WORKSPACE;
+  if (batch > 65535) return SV_ERR_UNSUPPORTED;
+  if (max_ctx_pages == 0) return SV_OK;
+  retr::SumParams p;
+  p.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
+  p.summ = static_cast<__nv_bfloat16*>(summaries);
+  p.block_table = block_table;
+  p.ctx_lens = ctx_lens;
+  p.first_page = first_page;
+  p.err = static_cast<int*>(workspace);
+  p.num_pages = num_pages;
+  p.num_kv_heads = num_kv_heads;
+  p.max_pages_per_seq = max_pages_per_seq;
+  const long long warps = static_cast<long long>(max_ctx_pages) * num_kv_heads;
+  const dim3 grid(static_cast<unsigned>((warps + retr::kWarpsPerCta - 1) / retr::kWarpsPerCta), batch, 1);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (head_dim == 128) retr::page_summary_kernel<128><<<grid, 256, 0, s>>>(p);
+  else retr::page_summary_kernel<64><<<grid, 256, 0, s>>>(p);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+sv_status sv_retrieve_pages_workspace_size(int batch, int num_kv_heads, int head_dim, int max_ctx_pages,
+                                           size_t* bytes) {
+  using namespace sv;
+  if (bytes == nullptr || batch < 1 || num_kv_heads < 1 || head_dim < 1 || max_ctx_pages < 0)
+    return SV_ERR_INVALID_ARG;
+  *bytes = kWorkspaceHeader +
+           align_up(static_cast<size_t>(batch) * num_kv_heads * 2 * head_dim * sizeof(float), 256) +
+           align_up(static_cast<size_t>(batch) * max_ctx_pages * sizeof(float), 256);
+  return SV_OK;
+}
+
+sv_status sv_retrieve_pages(const sv_retrieve_params* rp, sv_stream_t stream) {
+  using namespace sv;
+  if (rp == nullptr) return SV_ERR_INVALID_ARG;
+  const sv_retrieve_params& r = *rp;
+  if (!r.q || !r.summaries || !r.block_table || !r.ctx_lens || !r.cu_nodes || !r.kv_pages || !r.cu_kv_pages)
+    return SV_ERR_INVALID_ARG;
+  if (r.batch < 1 || r.num_q_heads < 1 || r.num_kv_heads < 1 || r.num_q_heads % r.num_kv_heads != 0 ||
+      r.num_pages < 1 || r.max_pages_per_seq < 1 || r.max_ctx_pages < 0 || r.sink_tokens < 0 ||
+      r.window_tokens < 0 || r.topk < 0 || r.reduce < SV_REDUCE_MEAN || r.reduce > SV_REDUCE_LAST ||
+      r.total_nodes < 1)
+    return SV_ERR_INVALID_ARG;
+  if (r.head_dim != 64 && r.head_dim != 128) return SV_ERR_UNSUPPORTED;
+  if (r.page_size != retr::kPage) return SV_ERR_UNSUPPORTED;
+  if (r.max_ctx_pages > retr::kMaxSortPages || r.max_ctx_pages > r.max_pages_per_seq) return SV_ERR_UNSUPPORTED;
+  if (!aligned16(r.q) || !aligned16(r.summaries)) return SV_ERR_INVALID_ARG;
+  const long long per_seq =
+      (r.sink_tokens + retr::kPage - 1) / retr::kPage + static_cast<long long>(r.topk) +
+      (r.window_tokens + retr::kPage - 1) / retr::kPage + 1;
+  if (r.kv_pages_capacity < static_cast<size_t>(r.batch) * static_cast<size_t>(
+                                std::min<long long>(per_seq, r.max_ctx_pages)))
+    return SV_ERR_INVALID_ARG;
+  size_t need = 0;
+  sv_retrieve_pages_workspace_size(r.batch, r.num_kv_heads, r.head_dim, r.max_ctx_pages, &need);
+  if (r.workspace == nullptr || r.workspace_bytes < need) return SV_ERR_WORKSPACE;
+  if (r.batch > 65535) return SV_ERR_UNSUPPORTED;
+  uint8_t* ws = static_cast<uint8_t*>(r.workspace);
+  float* qa = reinterpret_cast<float*>(ws + kWorkspaceHeader);
+  float* scores = r.scores != nullptr
+                      ? r.scores
+                      : reinterpret_cast<float*>(
+                            ws + kWorkspaceHeader +
+                            align_up(static_cast<size_t>(r.batch) * r.num_kv_heads * 2 * r.head_dim * sizeof(float),
+                                     256));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int G = r.num_q_heads / r.num_kv_heads;
+  const bool use_max = r.reduce == SV_REDUCE_MAX;
+  if (!use_max) {
+    retr::AggParams a;
+    a.q = static_cast<const __nv_bfloat16*>(r.q);
+    a.cu_nodes = r.cu_nodes;
+    a.qa = qa;
+    a.num_q_heads = r.num_q_heads;
+    a.group = G;
+    a.last_only = r.reduce == SV_REDUCE_LAST ? 1 : 0;
+    const dim3 grid(r.num_kv_heads, r.batch, 1);
+    if (r.head_dim == 128) retr::query_aggregate_kernel<128><<<grid, 128, 0, s>>>(a);
+    else retr::query_aggregate_kernel<64><<<grid, 64, 0, s>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  }
+  if (r.max_ctx_pages > 0) {
+    retr::ScoreParams sp;
+    sp.q = static_cast<const __nv_bfloat16*>(r.q);
+    sp.summ = static_cast<const __nv_bfloat16*>(r.summaries);
+    sp.qa = qa;
+    sp.block_table = r.block_table;
+    sp.ctx_lens = r.ctx_lens;
+    sp.cu_nodes = r.cu_nodes;
+    sp.scores = scores;
+    sp.err = reinterpret_cast<int*>(ws);
+    sp.num_pages = r.num_pages;
+    sp.num_q_heads = r.num_q_heads;
+    sp.num_kv_heads = r.num_kv_heads;
+    sp.group = G;
+    sp.max_pages_per_seq = r.max_pages_per_seq;
+    sp.max_ctx_pages = r.max_ctx_pages;
+    sp.sink_tokens = r.sink_tokens;
+    sp.window_tokens = r.window_tokens;
+    sp.reduce_max = use_max ? 1 : 0;
+    const dim3 grid((r.max_ctx_pages + retr::kWarpsPerCta - 1) / retr::kWarpsPerCta, r.batch, 1);
+    if (r.head_dim == 128) retr::page_score_kernel<128><<<grid, 256, 0, s>>>(sp);
+    else retr::page_score_kernel<64><<<grid, 256, 0, s>>>(sp);
+    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  }
+  retr::SelParams sel;
+  sel.scores = scores;
+  sel.ctx_lens = r.ctx_lens;
+  sel.kv_pages = r.kv_pages;
+  sel.cu_kv_pages = r.cu_kv_pages;
+  sel.err = reinterpret_cast<int*>(ws);
+  sel.batch = r.batch;
+  sel.max_ctx_pages = r.max_ctx_pages;
+  sel.sink_tokens = r.sink_tokens;
+  sel.window_tokens = r.window_tokens;
+  sel.topk = r.topk;
+  sel.sort_len = retr::pow2_at_least(std::max(1, r.max_ctx_pages));
+  const size_t smem = retr::select_smem_bytes(sel.sort_len);
+  if (cudaFuncSetAttribute(retr::select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return SV_ERR_CUDA;
+  retr::select_kernel<<<r.batch, retr::kSelThreads, smem, s>>>(sel);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -123,3 +123,32 @@ def test_commit_host_validation(lib):
     assert f(*args, None, None, 0, None) == 2
     args = base[:]
     assert f(*args, None, a, 8, None) == 4  # workspace too small
+
+
+def test_retrieval_host_validation(lib):
+    a = 1 << 20
+    n = binding.sv_retrieve_pages_workspace_size(2, 8, 128, 100)
+    assert n >= 256 + 2 * 8 * 2 * 128 * 4 + 2 * 100 * 4
+    base = dict(q=a, summaries=a, block_table=a, ctx_lens=a, cu_nodes=a, kv_pages=a, cu_kv_pages=a, batch=2,
+                num_q_heads=32, num_kv_heads=8, head_dim=128, num_pages=500, total_nodes=100,
+                max_pages_per_seq=200, max_ctx_pages=100, sink_tokens=64, window_tokens=256, topk=8,
+                kv_pages_capacity=2 * binding.retrieve_list_bound(64, 256, 8), workspace=a, workspace_bytes=n)
+
+    def call(**over):
+        kw = dict(base)
+        kw.update(over)
+        p = binding.make_retrieve_params(**kw)
+        return lib.sv_retrieve_pages(ctypes.byref(p), None)
+
+    assert call(head_dim=96) == 2
+    assert call(page_size=32) == 2
+    assert call(max_ctx_pages=20000, max_pages_per_seq=20000) == 2
+    assert call(kv_pages_capacity=10) == 1
+    assert call(workspace_bytes=16) == 4
+    assert call(reduce=3) == 1
+    assert call(q=None) == 1
+    assert call(num_q_heads=30) == 1
+    f = lib.sv_kv_page_summaries
+    assert f(None, 10, 8, 128, 16, a, 4, a, None, 1, 4, a, None, 0, None) == 1
+    assert f(a, 10, 8, 96, 16, a, 4, a, None, 1, 4, a, None, 0, None) == 2
+    assert f(a, 10, 8, 128, 16, a, 4, a, None, 1, 4, a, a, 8, None) == 4
