@@ -343,6 +343,51 @@ def run_reference(args):
 
 # ---------------------------------------------------------------------------- GPU leg
 
+def retrieval_timing(torch, st, args, world):
+    """SpecPV retrieval on the partial-KV workload (layer 0): the page
+    summaries of the whole context (built once per full verification) and one
+    retrieval (mean reduction, the workload's 64 sink tokens, 128 retrieved
+    pages = 32 blocks of 64 tokens, 1024-token window), each timed alone in a
+    CUDA graph."""
+    from speculative_decoding_tree_sv_gb300 import binding
+    c = st.case
+    mcp = int(max(1, (int(np.max(c.ctx_lens)) + 15) // 16))
+    summ = torch.zeros((c.num_pages, c.num_kv_heads, 2, c.head_dim), dtype=torch.bfloat16, device=st.dev)
+    sink, window, topk = 64, 1024, 128
+    cap = c.batch * binding.retrieve_list_bound(sink, window, topk)
+    kv = torch.empty(cap, dtype=torch.int32, device=st.dev)
+    cu = torch.empty(c.batch + 1, dtype=torch.int32, device=st.dev)
+    ws = torch.zeros(binding.sv_retrieve_pages_workspace_size(c.batch, c.num_kv_heads, c.head_dim, mcp),
+                     dtype=torch.uint8, device=st.dev)
+
+    def summaries():
+        binding.sv_kv_page_summaries(st.k_cache[0], c.num_pages, c.num_kv_heads, c.head_dim, st.block_table,
+                                     c.max_pages_per_seq, st.ctx_lens, None, c.batch, mcp, summ, ws)
+
+    params = binding.make_retrieve_params(
+        q=st.q[0], summaries=summ, block_table=st.block_table, ctx_lens=st.ctx_lens, cu_nodes=st.cu_nodes,
+        kv_pages=kv, cu_kv_pages=cu, batch=c.batch, num_q_heads=c.num_q_heads, num_kv_heads=c.num_kv_heads,
+        head_dim=c.head_dim, num_pages=c.num_pages, total_nodes=c.total_nodes,
+        max_pages_per_seq=c.max_pages_per_seq, max_ctx_pages=mcp, sink_tokens=sink, window_tokens=window,
+        topk=topk, workspace=ws)
+
+    def retrieve():
+        binding.sv_retrieve_pages(params)
+
+    ms_s, _ = _time_graph(torch, summaries, args.steps, args.warmup, world)
+    ms_r, _ = _time_graph(torch, retrieve, args.steps, args.warmup, world)
+    tokens = int(np.sum(c.ctx_lens))
+    pages = int(np.sum((c.ctx_lens + 15) // 16))
+    row = c.num_kv_heads * c.head_dim * 2                     # one token's K (bf16)
+    sum_bytes = tokens * row + pages * 2 * row                 # keys read, max/min written
+    cand = pages - c.batch * (sink // 16 + window // 16)
+    ret_bytes = cand * 2 * row + c.total_nodes * c.num_q_heads * c.head_dim * 2 + pages * 8
+    us_s, us_r = ms_s * 1e3 / args.steps, ms_r * 1e3 / args.steps
+    return {"summaries_us": us_s, "summaries_gbs": sum_bytes / (us_s * 1e-6) / 1e9,
+            "retrieve_us": us_r, "retrieve_gbs": ret_bytes / (us_r * 1e-6) / 1e9,
+            "reduce": "mean", "sink_tokens": sink, "window_tokens": window, "topk_pages": topk}
+
+
 def run_gpu(args):
     import torch
 
@@ -407,6 +452,8 @@ def run_gpu(args):
     ms_e2e, _ge = _time_graph(torch, e2e_step, args.steps, args.warmup, world)
     e2e_value = world * nodes_per_step / (ms_e2e * 1e-3 / args.steps)
 
+    retrieval = retrieval_timing(torch, st, args, world) if partial else None
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         s, detail = oracle_step_seconds(case, partial)
@@ -436,6 +483,7 @@ def run_gpu(args):
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": st.launches_per_step() * args.steps,
             "clocks": clocks,
+            **({"retrieval": retrieval} if retrieval else {}),
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -19,9 +19,9 @@
 // Kernels: page_summary_kernel (one warp per (page, KV head): max/min of the
 // page's valid keys, bf16), query_aggregate_kernel (averaged q+, q- per
 // (sequence, KV head)), page_score_kernel (one warp per page),
-// select_kernel (one CTA per sequence: bitonic sort of the candidates'
-// (score, page) keys in shared memory, top-k, then the sink, retrieved and
-// window pages written in ascending order).
+// select_kernel (one CTA per sequence: radix select of the k-th largest
+// importance, ties to the lower page, then the sink, retrieved and window
+// pages written in ascending order).
 #include <math.h>
 
 #include <algorithm>
@@ -32,7 +32,7 @@ namespace sv {
 namespace retr {
 
 constexpr int kPage = 16;
-constexpr int kMaxSortPages = 16384;  // candidate pages per sequence sorted in shared memory
+constexpr int kMaxSortPages = 16384;  // pages per sequence the selection holds in shared memory
 constexpr int kSelThreads = 1024;
 constexpr int kWarpsPerCta = 8;
 
@@ -148,29 +148,42 @@ struct AggParams {
 
 // The mean over the used queries of q+ and q-, split by KV head: the sum
 // over KV heads of qa . (kmax, kmin) is then the mean score.  One CTA per
-// (KV head, sequence), one thread per head dimension.
+// (KV head, sequence): 1024 threads, D per row slice, each slice summing
+// every R-th query row of the group before a shared-memory reduction.
 template <int D>
-__global__ void __launch_bounds__(D) query_aggregate_kernel(const __grid_constant__ AggParams p) {
+__global__ void __launch_bounds__(1024) query_aggregate_kernel(const __grid_constant__ AggParams p) {
+  constexpr int R = 1024 / D;  // row slices
+  __shared__ float red[2][R][D];
   const int kvh = blockIdx.x;
   const int b = blockIdx.y;
-  const int d = threadIdx.x;
+  const int d = threadIdx.x % D;
+  const int slice = threadIdx.x / D;
   const int n0 = p.cu_nodes[b];
   const int N = p.cu_nodes[b + 1] - n0;
   const int i0 = p.last_only ? max(0, N - 1) : 0;
   const int used = N - i0;
+  const int rows = used * p.group;
   float pos = 0.f, neg = 0.f;
-  for (int i = i0; i < N; ++i) {
-    const __nv_bfloat16* row = p.q + (static_cast<size_t>(n0 + i) * p.num_q_heads + kvh * p.group) * D + d;
-    for (int g = 0; g < p.group; ++g) {
-      const float v = __bfloat162float(row[static_cast<size_t>(g) * D]);
-      pos += fmaxf(v, 0.f);
-      neg += fminf(v, 0.f);
-    }
+#pragma unroll 4
+  for (int r = slice; r < rows; r += R) {
+    const int i = i0 + r / p.group, g = r % p.group;
+    const float v = __bfloat162float(p.q[(static_cast<size_t>(n0 + i) * p.num_q_heads + kvh * p.group + g) * D + d]);
+    pos += fmaxf(v, 0.f);
+    neg += fminf(v, 0.f);
   }
-  const float scale = used > 0 ? 1.f / (static_cast<float>(used) * p.num_q_heads) : 0.f;
-  float* dst = p.qa + (static_cast<size_t>(b) * gridDim.x + kvh) * 2 * D + d;
-  dst[0] = pos * scale;
-  dst[D] = neg * scale;
+  red[0][slice][d] = pos;
+  red[1][slice][d] = neg;
+  __syncthreads();
+  if (slice == 0) {
+    for (int s2 = 1; s2 < R; ++s2) {
+      pos += red[0][s2][d];
+      neg += red[1][s2][d];
+    }
+    const float scale = used > 0 ? 1.f / (static_cast<float>(used) * p.num_q_heads) : 0.f;
+    float* dst = p.qa + (static_cast<size_t>(b) * gridDim.x + kvh) * 2 * D + d;
+    dst[0] = pos * scale;
+    dst[D] = neg * scale;
+  }
 }
 
 // ------------------------------------------------------------------ scores
@@ -213,6 +226,7 @@ __global__ void __launch_bounds__(256) page_score_kernel(const __grid_constant__
     }
     if (!p.reduce_max) {
       float acc = 0.f;
+#pragma unroll 8
       for (int kvh = 0; kvh < p.num_kv_heads; ++kvh) {
         const __nv_bfloat16* s = p.summ + (static_cast<size_t>(phys) * p.num_kv_heads + kvh) * 2 * D + lane * E;
         const float* a = p.qa + (static_cast<size_t>(b) * p.num_kv_heads + kvh) * 2 * D + lane * E;
@@ -277,7 +291,6 @@ struct SelParams {
   int sink_tokens;
   int window_tokens;
   int topk;
-  int sort_len;  // power of two >= every sequence's candidate count
 };
 
 // Order-preserving map of a float to an unsigned integer.
@@ -286,11 +299,45 @@ __device__ __forceinline__ uint32_t ordered(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Block-wide exclusive prefix sum of one int per thread (kSelThreads).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* total) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = scratch[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    scratch[lane] = w;
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? scratch[warp - 1] : 0) + x - v;
+  if (total != nullptr) *total = scratch[kSelThreads / 32 - 1];
+  __syncthreads();
+  return before;
+}
+
+// One CTA per sequence.  The topk largest importances among the candidate
+// pages are found by a radix select on their order-preserving 32-bit codes
+// (four passes of eight bits): it yields the k-th largest code T and how
+// many pages with code T still belong to the top k, which are then the
+// lowest such pages.  Sink, retrieved and window pages are marked in a
+// bitmap and written in ascending order.
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_constant__ SelParams p) {
   extern __shared__ uint8_t smem_raw[];
-  unsigned long long* keys = reinterpret_cast<unsigned long long*>(smem_raw);
-  uint32_t* bits = reinterpret_cast<uint32_t*>(keys + p.sort_len);  // [kMaxSortPages / 32]
-  int* scan = reinterpret_cast<int*>(bits + kMaxSortPages / 32);    // [kSelThreads]
+  uint32_t* code = reinterpret_cast<uint32_t*>(smem_raw);           // [kMaxSortPages]
+  uint32_t* bits = code + kMaxSortPages;                             // [kMaxSortPages / 32]
+  int* hist = reinterpret_cast<int*>(bits + kMaxSortPages / 32);     // [256]
+  int* scratch = hist + 256;                                         // [32 + 4]
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
   if (tid == 0 && p.ctx_lens[b] > p.max_ctx_pages * kPage) report_error(p.err, SV_DEVERR_BAD_PAGE);
@@ -302,67 +349,85 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   int part = 0;
   for (int j = tid; j < b; j += kSelThreads)
     part += list_length(clamp_len(p.ctx_lens[j], p.max_ctx_pages), p.sink_tokens, p.window_tokens, p.topk);
-  scan[tid] = part;
-  __syncthreads();
-  for (int s = kSelThreads / 2; s > 0; s >>= 1) {
-    if (tid < s) scan[tid] += scan[tid + s];
-    __syncthreads();
-  }
-  const int offset = scan[0];
-  __syncthreads();
-  // keys: high word the ordered score, low word the inverted page, so one
-  // descending sort ranks by score and then by lower page
-  int n2 = 1;
-  while (n2 < ncand) n2 <<= 1;
-  for (int i = tid; i < n2; i += kSelThreads) {
-    unsigned long long key = 0ull;
-    if (i < ncand) {
-      const int page = rg.sink + i;
-      const float sc = p.scores[static_cast<size_t>(b) * p.max_ctx_pages + page];
-      key = (static_cast<unsigned long long>(ordered(sc)) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(page));
-    }
-    keys[i] = key;
-  }
+  int offset = 0;
+  block_exclusive_scan(part, scratch, &offset);
+  for (int i = tid; i < ncand; i += kSelThreads)
+    code[i] = ordered(p.scores[static_cast<size_t>(b) * p.max_ctx_pages + rg.sink + i]);
   for (int i = tid; i < kMaxSortPages / 32; i += kSelThreads) bits[i] = 0u;
-  __syncthreads();
-  for (int kk = 2; kk <= n2; kk <<= 1) {
-    for (int j = kk >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < n2; i += kSelThreads) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const unsigned long long a = keys[i], c = keys[ixj];
-          const bool desc = (i & kk) == 0;
-          if (desc ? (a < c) : (a > c)) {
-            keys[i] = c;
-            keys[ixj] = a;
+  // radix select of the k-th largest code
+  uint32_t prefix = 0u, mask = 0u;
+  int remaining = k;
+  volatile int* sel = scratch + 32;  // chosen digit, count above it
+  for (int shift = 24; shift >= 0 && k > 0; shift -= 8) {
+    for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < ncand; i += kSelThreads) {
+      const uint32_t c = code[i];
+      if ((c & mask) == prefix) atomicAdd(&hist[(c >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (tid < 32) {
+      // lane l holds digits 255 - 8l .. 248 - 8l (high digits first)
+      int cnt[8], sum = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        cnt[e] = hist[255 - 8 * tid - e];
+        sum += cnt[e];
+      }
+      int incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (tid >= o) incl += y;
+      }
+      int above = incl - sum;  // codes in higher digits than this lane's
+      const bool here = above < remaining && above + sum >= remaining;
+      if (here) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (above + cnt[e] >= remaining) {
+            sel[0] = 255 - 8 * tid - e;
+            sel[1] = above;
+            break;
           }
+          above += cnt[e];
         }
       }
-      __syncthreads();
     }
+    __syncthreads();
+    prefix |= static_cast<uint32_t>(sel[0]) << shift;
+    mask |= 255u << shift;
+    remaining -= sel[1];
+    __syncthreads();
   }
-  // mark the retrieved, sink and window pages, then write them in order
-  for (int i = tid; i < k; i += kSelThreads) {
-    const int page = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(keys[i] & 0xFFFFFFFFull));
-    atomicOr(&bits[page >> 5], 1u << (page & 31));
+  // codes above the threshold are retrieved; of those equal to it, the
+  // `remaining` lowest pages (candidates are stored in page order)
+  const int per = (ncand + kSelThreads - 1) / kSelThreads;
+  const int c0 = min(ncand, tid * per), c1 = min(ncand, c0 + per);
+  int eq = 0;
+  if (k > 0)
+    for (int i = c0; i < c1; ++i) eq += (code[i] == prefix) ? 1 : 0;
+  int eq_before = block_exclusive_scan(eq, scratch, nullptr);
+  if (k > 0) {
+    for (int i = c0; i < c1; ++i) {
+      const uint32_t c = code[i];
+      bool take = c > prefix;
+      if (c == prefix) take = eq_before++ < remaining;
+      if (take) {
+        const int page = rg.sink + i;
+        atomicOr(&bits[page >> 5], 1u << (page & 31));
+      }
+    }
   }
   for (int page = tid; page < rg.n_pages; page += kSelThreads)
     if (page < rg.sink || page >= rg.first_window) atomicOr(&bits[page >> 5], 1u << (page & 31));
   __syncthreads();
   const int words = (rg.n_pages + 31) / 32;
-  const int per = (words + kSelThreads - 1) / kSelThreads;  // words per thread
-  const int w0 = min(words, tid * per), w1 = min(words, w0 + per);
+  const int wper = (words + kSelThreads - 1) / kSelThreads;  // words per thread
+  const int w0 = min(words, tid * wper), w1 = min(words, w0 + wper);
   int cnt = 0;
   for (int w = w0; w < w1; ++w) cnt += __popc(bits[w]);
-  scan[tid] = cnt;
-  __syncthreads();
-  for (int s = 1; s < kSelThreads; s <<= 1) {  // inclusive scan
-    const int v = (tid >= s) ? scan[tid - s] : 0;
-    __syncthreads();
-    scan[tid] += v;
-    __syncthreads();
-  }
-  int pos = offset + scan[tid] - cnt;
+  int pos = offset + block_exclusive_scan(cnt, scratch, nullptr);
   for (int w = w0; w < w1; ++w) {
     uint32_t m = bits[w];
     while (m) {
@@ -377,15 +442,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   }
 }
 
-size_t select_smem_bytes(int sort_len) {
-  return static_cast<size_t>(sort_len) * 8 + kMaxSortPages / 8 + kSelThreads * 4;
-}
-
-int pow2_at_least(int n) {
-  int v = 1;
-  while (v < n) v <<= 1;
-  return v;
-}
+constexpr size_t kSelSmemBytes = kMaxSortPages * 4 + kMaxSortPages / 8 + 256 * 4 + 36 * 4;
 
 }  // namespace retr
 }  // namespace sv
@@ -480,8 +537,8 @@ sv_status sv_retrieve_pages(const sv_retrieve_params* rp, sv_stream_t stream) {
     a.group = G;
     a.last_only = r.reduce == SV_REDUCE_LAST ? 1 : 0;
     const dim3 grid(r.num_kv_heads, r.batch, 1);
-    if (r.head_dim == 128) retr::query_aggregate_kernel<128><<<grid, 128, 0, s>>>(a);
-    else retr::query_aggregate_kernel<64><<<grid, 64, 0, s>>>(a);
+    if (r.head_dim == 128) retr::query_aggregate_kernel<128><<<grid, 1024, 0, s>>>(a);
+    else retr::query_aggregate_kernel<64><<<grid, 1024, 0, s>>>(a);
     if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
   }
   if (r.max_ctx_pages > 0) {
@@ -519,12 +576,10 @@ sv_status sv_retrieve_pages(const sv_retrieve_params* rp, sv_stream_t stream) {
   sel.sink_tokens = r.sink_tokens;
   sel.window_tokens = r.window_tokens;
   sel.topk = r.topk;
-  sel.sort_len = retr::pow2_at_least(std::max(1, r.max_ctx_pages));
-  const size_t smem = retr::select_smem_bytes(sel.sort_len);
   if (cudaFuncSetAttribute(retr::select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess)
+                           static_cast<int>(retr::kSelSmemBytes)) != cudaSuccess)
     return SV_ERR_CUDA;
-  retr::select_kernel<<<r.batch, retr::kSelThreads, smem, s>>>(sel);
+  retr::select_kernel<<<r.batch, retr::kSelThreads, retr::kSelSmemBytes, s>>>(sel);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
