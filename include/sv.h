@@ -340,6 +340,50 @@ sv_status sv_retrieve_pages_workspace_size(int batch, int num_kv_heads, int head
 
 sv_status sv_retrieve_pages(const sv_retrieve_params* params, sv_stream_t stream);
 
+/* ------------------------------------------------------------------------
+ * SpecPV full / partial verification schedule.
+ *
+ * Defined by: SpecPV section 3.3 (partial verification begins after a full
+ * verification initialises the partial cache; the tokens accepted under
+ * partial verification sit in a buffer, and exceeding its limit triggers a
+ * full verification that refreshes the cache; before a full verification the
+ * partially verified tokens are prepended to the new candidates) and
+ * Appendix C (the limit is one verification step's tokens plus 20).
+ *
+ * Host bookkeeping per sequence.  A partial step attends the refresh's page
+ * list plus the pages the buffer has grown into (sv_partial_list_extend).  A
+ * full step re-verifies the buffer: its tree is the buffered tokens as a
+ * chain ahead of the new candidates, over the context as it was at the
+ * refresh (ctx_lens = refresh_ctx_len), attended in full; its commit
+ * rewrites the buffered slots with their exact K/V, then the summaries of
+ * the touched pages and the retrieval are refreshed.
+ * ---------------------------------------------------------------------- */
+typedef enum sv_verify_kind { SV_VERIFY_PARTIAL = 0, SV_VERIFY_FULL = 1 } sv_verify_kind;
+
+typedef struct sv_specpv_seq {
+  int has_partial_cache;  /* a full verification has built the partial cache */
+  int refresh_ctx_len;    /* committed length at that full verification        */
+  int buffer_tokens;      /* tokens committed by partial steps since            */
+} sv_specpv_seq;
+
+/* The verification the next step of a sequence needs, given the tokens that
+ * step can commit at most (the tree's depth + 1) and the buffer limit. */
+sv_verify_kind sv_specpv_next(const sv_specpv_seq* seq, int step_tokens, int buffer_limit);
+
+/* Updates the bookkeeping after a step of the given kind committed, leaving
+ * ctx_len_after committed tokens. */
+sv_status sv_specpv_after(sv_specpv_seq* seq, sv_verify_kind kind, int ctx_len_after);
+
+/* Partial lists between refreshes: sequence b's list made at the refresh
+ * (ref_pages[ref_cu[b] .. ref_cu[b+1]), for context length ref_ctx_lens[b])
+ * plus the logical pages ceil(ref_ctx_lens[b] / 16) .. ceil(ctx_lens[b] / 16)
+ * - 1 that the buffer has grown into; written packed, in sequence order, with
+ * prefix sums in cu_kv_pages [B+1].  kv_pages needs room for the refresh
+ * lists plus the new pages.  workspace optional (error word). */
+sv_status sv_partial_list_extend(const int* ref_pages, const int* ref_cu, const int* ref_ctx_lens,
+                                 const int* ctx_lens, int batch, int* kv_pages, int* cu_kv_pages,
+                                 void* workspace, size_t workspace_bytes, sv_stream_t stream);
+
 /* Diagnostics: per-CTA phase tracing of sv_tree_attention.
  *
  * After this call, every sv_tree_attention launch (until the buffer is

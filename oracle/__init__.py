@@ -32,6 +32,8 @@ from .attention import (  # noqa: F401
 from .accept import greedy_accept  # noqa: F401
 from .commit import kv_commit  # noqa: F401
 from .retrieval import (  # noqa: F401
+    extend_partial_lists,
+    specpv_schedule,
     block_importance,
     page_regions,
     page_summaries,

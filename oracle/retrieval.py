@@ -139,3 +139,40 @@ def retrieve_pages(q: np.ndarray, k_cache: np.ndarray, block_table: np.ndarray, 
         cu[b + 1] = cu[b] + len(lst)
     flat = np.array([p for lst in lists for p in lst], dtype=np.int32)
     return flat, cu, scores_all
+
+
+def extend_partial_lists(ref_pages: Sequence[int], ref_cu: Sequence[int], ref_ctx_lens: Sequence[int],
+                         ctx_lens: Sequence[int], page_size: int = 16) -> Tuple[np.ndarray, np.ndarray]:
+    """SpecPV section 3.3: between refreshes a sequence attends its refresh
+    list plus the pages its buffer of partially verified tokens has grown
+    into (the buffer follows the window at the end of the context)."""
+    lists = []
+    for b in range(len(ctx_lens)):
+        lst = [int(x) for x in ref_pages[ref_cu[b]:ref_cu[b + 1]]]
+        first_new = (int(ref_ctx_lens[b]) + page_size - 1) // page_size
+        now = (int(ctx_lens[b]) + page_size - 1) // page_size
+        lists.append(lst + list(range(first_new, now)))
+    cu = np.zeros(len(lists) + 1, dtype=np.int32)
+    for b, lst in enumerate(lists):
+        cu[b + 1] = cu[b] + len(lst)
+    return np.array([p for lst in lists for p in lst], dtype=np.int32), cu
+
+
+def specpv_schedule(step_commits: Sequence[int], step_tokens: int, buffer_limit: int,
+                    ctx_len0: int) -> List[str]:
+    """Kinds of verification a sequence runs (SpecPV section 3.3): full until
+    a partial cache exists; partial while the buffer of tokens committed by
+    partial steps, plus what the next step can commit, fits the limit; full
+    (refreshing the cache, emptying the buffer) otherwise.  step_commits[i]
+    is what step i commits."""
+    kinds, has_cache, refresh_len, ctx = [], False, 0, int(ctx_len0)
+    for c in step_commits:
+        buffered = ctx - refresh_len
+        if not has_cache or buffered + step_tokens > buffer_limit:
+            kinds.append("full")
+            ctx += int(c)
+            has_cache, refresh_len = True, ctx
+        else:
+            kinds.append("partial")
+            ctx += int(c)
+    return kinds

@@ -60,6 +60,11 @@ class sv_retrieve_params(ctypes.Structure):
 
 
 SV_REDUCE_MEAN, SV_REDUCE_MAX, SV_REDUCE_LAST = 0, 1, 2
+SV_VERIFY_PARTIAL, SV_VERIFY_FULL = 0, 1
+
+
+class sv_specpv_seq(ctypes.Structure):
+    _fields_ = [("has_partial_cache", c_int), ("refresh_ctx_len", c_int), ("buffer_tokens", c_int)]
 
 _LIB = None
 
@@ -104,6 +109,13 @@ def load(path: Optional[str] = None):
     lib.sv_retrieve_pages_workspace_size.argtypes = [c_int, c_int, c_int, c_int, P(c_size_t)]
     lib.sv_retrieve_pages.restype = c_int
     lib.sv_retrieve_pages.argtypes = [P(sv_retrieve_params), c_void_p]
+    lib.sv_partial_list_extend.restype = c_int
+    lib.sv_partial_list_extend.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p,
+                                           c_void_p, c_size_t, c_void_p]
+    lib.sv_specpv_next.restype = c_int
+    lib.sv_specpv_next.argtypes = [P(sv_specpv_seq), c_int, c_int]
+    lib.sv_specpv_after.restype = c_int
+    lib.sv_specpv_after.argtypes = [P(sv_specpv_seq), c_int, c_int]
     lib.sv_set_trace_buffer.restype = c_int
     lib.sv_set_trace_buffer.argtypes = [c_void_p, c_size_t]
     lib.sv_get_device_error.restype = c_int
@@ -290,6 +302,23 @@ def make_retrieve_params(*, q, summaries, block_table, ctx_lens, cu_nodes, kv_pa
 
 def sv_retrieve_pages(params: sv_retrieve_params, stream=None) -> None:
     _check(load().sv_retrieve_pages(ctypes.byref(params), _stream(stream)), "sv_retrieve_pages")
+
+
+def sv_partial_list_extend(ref_pages, ref_cu, ref_ctx_lens, ctx_lens, batch: int, kv_pages, cu_kv_pages,
+                           workspace=None, workspace_bytes: int = 0, stream=None) -> None:
+    if workspace is not None and not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(load().sv_partial_list_extend(_ptr(ref_pages), _ptr(ref_cu), _ptr(ref_ctx_lens), _ptr(ctx_lens), batch,
+                                         _ptr(kv_pages), _ptr(cu_kv_pages), _ptr(workspace), workspace_bytes,
+                                         _stream(stream)), "sv_partial_list_extend")
+
+
+def sv_specpv_next(seq: sv_specpv_seq, step_tokens: int, buffer_limit: int) -> int:
+    return int(load().sv_specpv_next(ctypes.byref(seq), step_tokens, buffer_limit))
+
+
+def sv_specpv_after(seq: sv_specpv_seq, kind: int, ctx_len_after: int) -> None:
+    _check(load().sv_specpv_after(ctypes.byref(seq), kind, ctx_len_after), "sv_specpv_after")
 
 
 TRACE_SLOTS = 16

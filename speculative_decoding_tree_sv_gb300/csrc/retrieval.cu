@@ -444,10 +444,97 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
 
 constexpr size_t kSelSmemBytes = kMaxSortPages * 4 + kMaxSortPages / 8 + 256 * 4 + 36 * 4;
 
+// ------------------------------------------------------------------ list extension
+
+struct ExtendParams {
+  const int* ref_pages;  // the lists made at the last refresh
+  const int* ref_cu;
+  const int* ref_ctx_lens;
+  const int* ctx_lens;
+  int* kv_pages;
+  int* cu_kv_pages;
+  int* err;
+};
+
+// The partial cache between refreshes: the refresh's list plus every page
+// the buffer of partially verified tokens has grown into since (SpecPV
+// section 3.3).  One CTA per sequence; the start of its list is the sum of
+// the earlier sequences' lengths.
+__device__ __forceinline__ int extended_length(const ExtendParams& p, int j) {
+  const int n_ref = p.ref_cu[j + 1] - p.ref_cu[j];
+  const int ref_pages = (p.ref_ctx_lens[j] + kPage - 1) / kPage;
+  const int now_pages = (p.ctx_lens[j] + kPage - 1) / kPage;
+  return n_ref + max(0, now_pages - max(ref_pages, 0));
+}
+
+__global__ void __launch_bounds__(256) list_extend_kernel(const __grid_constant__ ExtendParams p) {
+  __shared__ int red[256];
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  int part = 0;
+  for (int j = tid; j < b; j += blockDim.x) part += extended_length(p, j);
+  red[tid] = part;
+  __syncthreads();
+  for (int s = blockDim.x / 2; s > 0; s >>= 1) {
+    if (tid < s) red[tid] += red[tid + s];
+    __syncthreads();
+  }
+  const int offset = red[0];
+  const int r0 = p.ref_cu[b], n_ref = p.ref_cu[b + 1] - r0;
+  const int ref_pages = (p.ref_ctx_lens[b] + kPage - 1) / kPage;
+  const int now_pages = (p.ctx_lens[b] + kPage - 1) / kPage;
+  if (tid == 0 && p.ctx_lens[b] < p.ref_ctx_lens[b]) report_error(p.err, SV_DEVERR_BAD_PAGE);
+  for (int i = tid; i < n_ref; i += blockDim.x) p.kv_pages[offset + i] = p.ref_pages[r0 + i];
+  for (int i = tid; i < now_pages - ref_pages; i += blockDim.x) p.kv_pages[offset + n_ref + i] = ref_pages + i;
+  if (tid == 0) {
+    p.cu_kv_pages[b + 1] = offset + n_ref + max(0, now_pages - ref_pages);
+    if (b == 0) p.cu_kv_pages[0] = 0;
+  }
+}
+
 }  // namespace retr
 }  // namespace sv
 
 extern "C" {
+
+sv_status sv_partial_list_extend(const int* ref_pages, const int* ref_cu, const int* ref_ctx_lens,
+                                 const int* ctx_lens, int batch, int* kv_pages, int* cu_kv_pages,
+                                 void* workspace, size_t workspace_bytes, sv_stream_t stream) {
+  using namespace sv;
+  if (!ref_pages || !ref_cu || !ref_ctx_lens || !ctx_lens || !kv_pages || !cu_kv_pages || batch < 1)
+    return SV_ERR_INVALID_ARG;
+  if (workspace != nullptr && workspace_bytes < kWorkspaceHeader) return SV_ERR_WORKSPACE;
+  retr::ExtendParams p;
+  p.ref_pages = ref_pages;
+  p.ref_cu = ref_cu;
+  p.ref_ctx_lens = ref_ctx_lens;
+  p.ctx_lens = ctx_lens;
+  p.kv_pages = kv_pages;
+  p.cu_kv_pages = cu_kv_pages;
+  p.err = static_cast<int*>(workspace);
+  retr::list_extend_kernel<<<batch, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+sv_verify_kind sv_specpv_next(const sv_specpv_seq* seq, int step_tokens, int buffer_limit) {
+  if (seq == nullptr || !seq->has_partial_cache) return SV_VERIFY_FULL;
+  return seq->buffer_tokens + step_tokens > buffer_limit ? SV_VERIFY_FULL : SV_VERIFY_PARTIAL;
+}
+
+sv_status sv_specpv_after(sv_specpv_seq* seq, sv_verify_kind kind, int ctx_len_after) {
+  if (seq == nullptr || ctx_len_after < 0) return SV_ERR_INVALID_ARG;
+  if (kind == SV_VERIFY_FULL) {
+    seq->has_partial_cache = 1;
+    seq->refresh_ctx_len = ctx_len_after;
+    seq->buffer_tokens = 0;
+    return SV_OK;
+  }
+  if (kind != SV_VERIFY_PARTIAL || !seq->has_partial_cache || ctx_len_after < seq->refresh_ctx_len)
+    return SV_ERR_INVALID_ARG;
+  seq->buffer_tokens = ctx_len_after - seq->refresh_ctx_len;
+  return SV_OK;
+}
+
 
 sv_status sv_kv_page_summaries(const void* k_cache, int num_pages, int num_kv_heads, int head_dim, int page_size,
                                const int* block_table, int max_pages_per_seq, const int* ctx_lens,

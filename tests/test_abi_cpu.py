@@ -7,6 +7,7 @@ import os
 import re
 import subprocess
 
+import numpy as np
 import pytest
 
 from speculative_decoding_tree_sv_gb300 import binding, build
@@ -152,3 +153,24 @@ def test_retrieval_host_validation(lib):
     assert f(None, 10, 8, 128, 16, a, 4, a, None, 1, 4, a, None, 0, None) == 1
     assert f(a, 10, 8, 96, 16, a, 4, a, None, 1, 4, a, None, 0, None) == 2
     assert f(a, 10, 8, 128, 16, a, 4, a, None, 1, 4, a, a, 8, None) == 4
+
+
+def test_specpv_schedule_matches_the_oracle(lib):
+    import oracle
+    rng = np.random.default_rng(0)
+    for trial in range(50):
+        step_tokens = int(rng.integers(1, 10))
+        limit = step_tokens + int(rng.integers(0, 30))
+        commits = rng.integers(1, step_tokens + 1, size=20)
+        want = oracle.specpv_schedule(commits, step_tokens, limit, ctx_len0=500)
+        seq = binding.sv_specpv_seq()
+        ctx, got = 500, []
+        for c in commits:
+            kind = binding.sv_specpv_next(seq, step_tokens, limit)
+            got.append("full" if kind == binding.SV_VERIFY_FULL else "partial")
+            ctx += int(c)
+            binding.sv_specpv_after(seq, kind, ctx)
+        assert got == want, trial
+    seq = binding.sv_specpv_seq()
+    with pytest.raises(binding.SvError):
+        binding.sv_specpv_after(seq, binding.SV_VERIFY_PARTIAL, 10)  # no partial cache yet

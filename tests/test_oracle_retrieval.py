@@ -157,3 +157,25 @@ def test_planted_mistake_is_caught():
         if wrong < max(float(q @ k) for k in keys) - 1e-12:
             broken += 1
     assert broken > 0
+
+
+def test_schedule_full_then_partial_until_the_buffer_overflows():
+    # SpecPV Appendix C: the limit is one step's tokens plus 20
+    step_tokens, limit = 8, 8 + 20
+    kinds = oracle.specpv_schedule([5] * 12, step_tokens, limit, ctx_len0=1000)
+    # after a full step the buffer grows by 5 per partial step; a partial
+    # step needs buffered + 8 <= 28 (only exceeding the limit forces a full
+    # step), so five partial steps (0, 5, 10, 15, 20 buffered) fit and the
+    # next (25 + 8 > 28) is full again
+    assert kinds == ["full"] + ["partial"] * 5 + ["full"] + ["partial"] * 5
+
+
+def test_schedule_limit_below_one_step_is_always_full():
+    assert oracle.specpv_schedule([3] * 5, 8, 7, 100) == ["full"] * 5
+
+
+def test_extended_lists_append_the_buffer_pages():
+    kv, cu = oracle.extend_partial_lists([0, 5, 9, 10, 1, 2], [0, 4, 6], [170, 40], [200, 40])
+    # sequence 0: pages 0..10 at the refresh (last page 10), now 13 pages
+    assert kv[cu[0]:cu[1]].tolist() == [0, 5, 9, 10, 11, 12]
+    assert kv[cu[1]:cu[2]].tolist() == [1, 2]
