@@ -6,15 +6,24 @@
 // choice at its parent and its parent is accepted.  The deepest accepted node
 // wins; equal depths go to the lexicographically smallest root path.
 //
-// One launch: CTAs stream vocabulary chunks of one row (16-byte loads) and
-// fold their (value, index) maximum into a per-row 64-bit key with atomicMax
+// One launch, one CTA per (16384-entry vocabulary chunk, row).  A CTA asks
+// for its whole chunk at once: the first half with 16-byte asynchronous
+// copies into shared memory (cp.async), the second half with 16-byte loads
+// into registers.  Holding half of the chunk in shared memory keeps the
+// registers per thread low enough that every CTA of a Llama-sized step
+// (60 rows x 8 chunks) is resident, so the whole logits tensor is in flight
+// in one wave; for larger steps each SM keeps five CTAs' 64 KB in flight.  The CTA
+// folds its (value, index) maximum into a per-row 64-bit key with atomicMax
 // (order-preserving float bits in the high word, inverted index in the low
 // word, so the lowest index wins ties).  The last CTA to finish a sequence
-// (atomic ticket, no waiting) walks that sequence's tree with one warp:
-// pointer jumping gives every node its depth, its accepted flag and its
-// ancestor set in log2(128) rounds, then a short top-down walk picks the
-// lexicographically smallest deepest path.  It resets the keys and the
-// ticket so the workspace is ready for the next call.
+// (atomic ticket, no waiting) walks that sequence's tree with all its
+// threads, one node per thread: pointer jumping gives every node its depth,
+// its accepted flag and its ancestor set in at most log2(128) rounds, then a
+// short top-down walk picks the lexicographically smallest deepest path.  It
+// resets the keys and the ticket so the workspace is ready for the next call.
+//
+// Rows that do not start on a 16-byte boundary (vocabulary not a multiple of
+// 4, or an unaligned logits pointer) are read with plain loads.
 #include <mutex>
 
 #include "sv_device.cuh"
@@ -23,7 +32,10 @@ namespace sv {
 namespace acc {
 
 constexpr int kThreads = 256;
-constexpr int kChunk = 8192;  // vocabulary entries per CTA (8 float4 per thread)
+constexpr int kSmemPart = 8192;  // entries copied into shared memory (8 x 16 B per thread)
+constexpr int kRegPart = 8192;   // entries loaded into registers (8 float4 per thread)
+constexpr int kChunk = kSmemPart + kRegPart;
+constexpr uint32_t kDynSmem = kSmemPart * 4;  // the shared-memory part, later the tree walk's arrays
 
 __device__ __forceinline__ unsigned long long pack_key(float v, int idx) {
   if (v == 0.0f) v = 0.0f;  // -0.0 and +0.0 compare equal
@@ -58,135 +70,178 @@ struct Params {
   bool vec4;
 };
 
-// Tree walk of sequence b by one warp (N <= 128 nodes, 4 per lane).
-__device__ void walk_sequence(const Params& p, int b, int n0, int N) {
-  __shared__ int s_am[128], s_par[128], s_ptr[2][128], s_dep[2][128];
-  __shared__ uint32_t s_acc[2][128];
-  __shared__ uint32_t s_anc[2][128][4];
-  const int lane = threadIdx.x & 31;
-  if (N < 1 || N > kMaxNodes) {
-    report_error(p.err, SV_DEVERR_BAD_TREE);
-    if (lane == 0) p.tickets[b] = 0;
+// Tree walk of sequence b (nodes n0 .. n0 + N - 1) by the whole CTA, one node
+// per thread; `scratch` is 8 KB of shared memory nothing else uses now.
+__device__ void walk_sequence(const Params& p, int b, int n0, int N, uint8_t* scratch) {
+  int* s_am = reinterpret_cast<int*>(scratch);                  // [128]
+  int* s_par = s_am + kMaxNodes;                                // [128]
+  int* s_ptr = s_par + kMaxNodes;                               // [2][128]
+  int* s_dep = s_ptr + 2 * kMaxNodes;                           // [2][128]
+  uint32_t* s_acc = reinterpret_cast<uint32_t*>(s_dep + 2 * kMaxNodes);  // [2][128]
+  uint32_t* s_anc = s_acc + 2 * kMaxNodes;                      // [2][128][4]
+  uint32_t* s_good = s_anc + 2 * kMaxNodes * 4;                 // [4]
+  int* s_best = reinterpret_cast<int*>(s_good + 4);
+  const int t = threadIdx.x;
+  if (N < 1 || N > kMaxNodes) {  // uniform over the CTA
+    if (t == 0) {
+      report_error(p.err, SV_DEVERR_BAD_TREE);
+      p.tickets[b] = 0;
+    }
     return;
   }
-
-  for (int n = lane; n < N; n += 32) {
-    const unsigned long long k = atomicExch(p.keys + n0 + n, 0ull);  // read and reset
-    s_am[n] = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull));
-    int par = (n == 0) ? -1 : p.parents[n0 + n];
-    if (n != 0 && (par < 0 || par >= n)) {
-      report_error(p.err, SV_DEVERR_BAD_PARENT);
-      par = 0;
+  if (t < 4) s_good[t] = 0u;
+  if (t == 0) *s_best = 0;
+  int am = 0, par = -1, tok = 0;
+  if (t < N) {
+    // the keys were last written by atomics at L2: read them there, then reset
+    const unsigned long long k = __ldcg(p.keys + n0 + t);
+    p.keys[n0 + t] = 0ull;
+    am = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull));
+    if (t != 0) {
+      par = p.parents[n0 + t];
+      tok = p.tokens[n0 + t];
+      if (par < 0 || par >= t) {
+        report_error(p.err, SV_DEVERR_BAD_PARENT);
+        par = 0;
+      }
     }
-    s_par[n] = par;
+    s_am[t] = am;
+    s_par[t] = par;
   }
-  __syncwarp();
-  for (int n = lane; n < N; n += 32) {
-    const int par = s_par[n];
-    const bool matched = (n == 0) || (p.tokens[n0 + n] == s_am[par]);
-    s_ptr[0][n] = (n == 0) ? 0 : par;
-    s_dep[0][n] = (n == 0) ? 0 : 1;
-    s_acc[0][n] = matched ? 1u : 0u;
-    uint32_t a[4] = {0, 0, 0, 0};
-    a[n >> 5] |= 1u << (n & 31);
-    if (n != 0) a[par >> 5] |= 1u << (par & 31);
+  __syncthreads();
+  if (t < N) {
+    const bool matched = (t == 0) || (tok == s_am[par]);
+    s_ptr[t] = (t == 0) ? 0 : par;
+    s_dep[t] = (t == 0) ? 0 : 1;
+    s_acc[t] = matched ? 1u : 0u;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) s_anc[0][n][w] = a[w];
-    if (p.argmax_out != nullptr) p.argmax_out[n0 + n] = s_am[n];
+    for (int w = 0; w < 4; ++w) {
+      uint32_t a = ((t >> 5) == w) ? (1u << (t & 31)) : 0u;
+      if (t != 0 && (par >> 5) == w) a |= 1u << (par & 31);
+      s_anc[t * 4 + w] = a;
+    }
+    if (p.argmax_out != nullptr) p.argmax_out[n0 + t] = am;
   }
-  __syncwarp();
   // pointer jumping: after round r, ptr = 2^(r+1)-th ancestor (clamped at
   // the root), dep = distance to it, acc = all matched on the way, anc =
-  // every node within that distance.
+  // every node within that distance; done once every pointer is the root
   int cur = 0;
-  for (int round = 0; round < 7; ++round) {
+  for (int round = 0;; ++round) {
+    const int settled = __syncthreads_and(t >= N || s_ptr[cur * kMaxNodes + t] == 0);
+    if (settled || round == 7) break;
     const int nxt = cur ^ 1;
-    for (int n = lane; n < N; n += 32) {
-      const int q = s_ptr[cur][n];
-      s_ptr[nxt][n] = s_ptr[cur][q];
-      s_dep[nxt][n] = s_dep[cur][n] + s_dep[cur][q];
-      s_acc[nxt][n] = s_acc[cur][n] & s_acc[cur][q];
+    if (t < N) {
+      const int q = s_ptr[cur * kMaxNodes + t];
+      s_ptr[nxt * kMaxNodes + t] = s_ptr[cur * kMaxNodes + q];
+      s_dep[nxt * kMaxNodes + t] = s_dep[cur * kMaxNodes + t] + s_dep[cur * kMaxNodes + q];
+      s_acc[nxt * kMaxNodes + t] = s_acc[cur * kMaxNodes + t] & s_acc[cur * kMaxNodes + q];
 #pragma unroll
-      for (int w = 0; w < 4; ++w) s_anc[nxt][n][w] = s_anc[cur][n][w] | s_anc[cur][q][w];
+      for (int w = 0; w < 4; ++w)
+        s_anc[(nxt * kMaxNodes + t) * 4 + w] = s_anc[(cur * kMaxNodes + t) * 4 + w] | s_anc[(cur * kMaxNodes + q) * 4 + w];
     }
-    __syncwarp();
     cur = nxt;
   }
-  // deepest accepted depth
-  int best = 0;
-  for (int n = lane; n < N; n += 32)
-    if (s_acc[cur][n]) best = max(best, s_dep[cur][n]);
+  // deepest accepted depth, then the nodes lying on some deepest accepted path
+  const bool acc = t < N && s_acc[cur * kMaxNodes + t] != 0u;
+  const int dep = acc ? s_dep[cur * kMaxNodes + t] : 0;
+  if (acc && dep > 0) atomicMax(s_best, dep);
+  __syncthreads();
+  const int best = *s_best;
+  if (acc && dep == best) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
-  // nodes lying on some deepest accepted path
-  uint32_t good[4] = {0, 0, 0, 0};
-  for (int n = lane; n < N; n += 32)
-    if (s_acc[cur][n] && s_dep[cur][n] == best) {
-#pragma unroll
-      for (int w = 0; w < 4; ++w) good[w] |= s_anc[cur][n][w];
+    for (int w = 0; w < 4; ++w) {
+      const uint32_t a = s_anc[(cur * kMaxNodes + t) * 4 + w];
+      if (a != 0u) atomicOr(s_good + w, a);
     }
-#pragma unroll
-  for (int w = 0; w < 4; ++w)
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) good[w] |= __shfl_xor_sync(0xffffffffu, good[w], o);
-  // top-down: smallest-index child on a deepest path, depth by depth
-  if (best > p.max_depth) report_error(p.err, SV_DEVERR_DEPTH);
+  }
+  __syncthreads();
+  if (t >= 32) return;
+  // top-down (one warp): smallest-index child on a deepest path, depth by depth
+  const int lane = t;
+  if (lane == 0 && best > p.max_depth) report_error(p.err, SV_DEVERR_DEPTH);
   int* out_path = p.accepted_nodes + static_cast<size_t>(b) * (p.max_depth + 1);
-  int node = 0;
+  int node = 0, len = best;
   if (lane == 0) out_path[0] = 0;
   for (int d = 1; d <= best; ++d) {
     int pick = 0x7FFFFFFF;
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
       const int n = lane + 32 * s;
-      const bool c = n < N && n != 0 && s_par[n] == node && ((good[s] >> lane) & 1u);
+      const bool c = n < N && n != 0 && s_par[n] == node && ((s_good[s] >> lane) & 1u);
       const uint32_t bal = __ballot_sync(0xffffffffu, c);
       if (bal != 0 && pick == 0x7FFFFFFF) pick = 32 * s + (__ffs(bal) - 1);
     }
     if (pick == 0x7FFFFFFF) {  // unreachable for a well-formed tree
-      report_error(p.err, SV_DEVERR_BAD_TREE);
-      best = d - 1;
+      if (lane == 0) report_error(p.err, SV_DEVERR_BAD_TREE);
+      len = d - 1;
       break;
     }
     node = pick;
     if (lane == 0 && d <= p.max_depth) out_path[d] = node;
   }
-  for (int d = best + 1 + lane; d <= p.max_depth; d += 32) out_path[d] = -1;
+  for (int d = len + 1 + lane; d <= p.max_depth; d += 32) out_path[d] = -1;
   if (lane == 0) {
-    p.accept_len[b] = best;
+    p.accept_len[b] = len;
     p.bonus[b] = s_am[node];
     p.tickets[b] = 0;
   }
 }
 
 __global__ void __launch_bounds__(kThreads) greedy_accept_kernel(const __grid_constant__ Params p) {
-  const int row = blockIdx.y;
-  const int chunk = blockIdx.x;
-  __shared__ int s_b, s_last;
+  extern __shared__ __align__(128) uint8_t dyn[];  // [kSmemPart] floats, then the walk's arrays
+  __shared__ int s_b, s_n0, s_n, s_last;
   __shared__ float s_v[kThreads / 32];
   __shared__ int s_i[kThreads / 32];
-
+  const int row = blockIdx.y;
+  const int chunk = blockIdx.x;
   const int lo = chunk * kChunk;
   const int hi = min(p.vocab, lo + kChunk);
+  const int smem_hi = min(hi, lo + kSmemPart);  // shared-memory part [lo, smem_hi), registers [lo + kSmemPart, hi)
   const float* rowp = p.logits + static_cast<size_t>(row) * p.vocab;
+  const int n4s = (smem_hi - lo) >> 2;  // float4 of the shared-memory part
+  if (p.vec4) {
+#pragma unroll
+    for (int u = 0; u < kSmemPart / (4 * kThreads); ++u) {
+      const int j = threadIdx.x + u * kThreads;
+      if (j < n4s)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dyn + 16 * j)),
+                     "l"(rowp + lo + 4 * j) : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
   float bv = -INFINITY;
   int bi = 0x7FFFFFFF;
   if (p.vec4) {
     const float4* r4 = reinterpret_cast<const float4*>(rowp);
-    float4 v[kChunk / (4 * kThreads)];
+    float4 v[kRegPart / (4 * kThreads)];
 #pragma unroll
-    for (int u = 0; u < kChunk / (4 * kThreads); ++u) {
-      const int e = lo + 4 * (threadIdx.x + u * kThreads);
+    for (int u = 0; u < kRegPart / (4 * kThreads); ++u) {
+      const int e = lo + kSmemPart + 4 * (threadIdx.x + u * kThreads);
       v[u] = (e < hi) ? __ldcs(r4 + (e >> 2)) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     }
 #pragma unroll
-    for (int u = 0; u < kChunk / (4 * kThreads); ++u) {
-      const int e = lo + 4 * (threadIdx.x + u * kThreads);
+    for (int u = 0; u < kRegPart / (4 * kThreads); ++u) {
+      const int e = lo + kSmemPart + 4 * (threadIdx.x + u * kThreads);
       if (e < hi) {
         take(v[u].x, e, bv, bi);
         take(v[u].y, e + 1, bv, bi);
         take(v[u].z, e + 2, bv, bi);
         take(v[u].w, e + 3, bv, bi);
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();  // every thread's copies have landed
+    const float4* b4 = reinterpret_cast<const float4*>(dyn);
+#pragma unroll
+    for (int u = 0; u < kSmemPart / (4 * kThreads); ++u) {
+      const int j = threadIdx.x + u * kThreads;
+      if (j < n4s) {
+        const float4 w = b4[j];
+        const int e = lo + 4 * j;
+        take(w.x, e, bv, bi);
+        take(w.y, e + 1, bv, bi);
+        take(w.z, e + 2, bv, bi);
+        take(w.w, e + 3, bv, bi);
       }
     }
   } else {
@@ -214,19 +269,19 @@ __global__ void __launch_bounds__(kThreads) greedy_accept_kernel(const __grid_co
       if (p.cu_nodes[mid] <= row) lo_b = mid;
       else hi_b = mid;
     }
+    const int n0 = p.cu_nodes[lo_b];
+    const int n_rows = p.cu_nodes[lo_b + 1] - n0;
     s_b = lo_b;
-    const int n_rows = p.cu_nodes[lo_b + 1] - p.cu_nodes[lo_b];
+    s_n0 = n0;
+    s_n = n_rows;
     __threadfence();
     const int ticket = atomicAdd(p.tickets + lo_b, 1);
     s_last = (ticket == n_rows * p.chunks - 1);
   }
   __syncthreads();
-  if (s_last && warp == 0) {
+  if (s_last) {
     __threadfence();
-    const int b = s_b;
-    const int n0 = p.cu_nodes[b];
-    const int N = p.cu_nodes[b + 1] - n0;
-    walk_sequence(p, b, n0, N);
+    walk_sequence(p, s_b, s_n0, s_n, dyn);
   }
 }
 
@@ -274,7 +329,7 @@ sv_status sv_greedy_accept(const float* logits, int vocab, const int* tokens, co
   p.max_depth = max_depth;
   p.vec4 = (vocab % 4 == 0) && sv::aligned16(logits);
   dim3 grid(p.chunks, total_nodes);
-  sv::acc::greedy_accept_kernel<<<grid, sv::acc::kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  sv::acc::greedy_accept_kernel<<<grid, sv::acc::kThreads, sv::acc::kDynSmem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
   if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
   return SV_OK;
 }

@@ -119,6 +119,34 @@ def test_full_size_logits_planted_paths():
         _assert_accept_equal(run_accept(case), ref, case)
 
 
+def test_workspace_reused_across_calls_and_unaligned_rows():
+    """One workspace serves consecutive calls (the kernel resets its keys and
+    tickets), and logits whose rows do not start on a 16-byte boundary take
+    the plain-load path with the same answers."""
+    case = make_case("serving_mix", ctx=16)
+    ref = oracle.greedy_accept(case.logits, case.tokens, case.parents, case.cu_nodes)
+    T, V, B = case.total_nodes, case.vocab, case.batch
+    dev = "cuda"
+    tokens, parents, cu = i32(case.tokens), i32(case.parents), i32(case.cu_nodes)
+    ws = torch.zeros(binding.sv_greedy_accept_workspace_size(B, T), dtype=torch.uint8, device=dev)
+    flat = torch.empty(T * V + 1, dtype=torch.float32, device=dev)
+    flat[1:] = torch.from_numpy(case.logits).reshape(-1).to(dev)
+    aligned = torch.from_numpy(case.logits).to(dev)
+    for logits in (aligned, flat[1:].view(T, V), aligned):
+        am = torch.full((T,), -7, dtype=torch.int32, device=dev)
+        alen = torch.full((B,), -7, dtype=torch.int32, device=dev)
+        anodes = torch.full((B, case.max_depth + 1), -7, dtype=torch.int32, device=dev)
+        bonus = torch.full((B,), -7, dtype=torch.int32, device=dev)
+        binding.sv_greedy_accept(logits, V, tokens, parents, cu, B, T, case.max_nodes, case.max_depth, am, alen,
+                                 anodes, bonus, ws)
+        torch.cuda.synchronize()
+        res = dict(argmax=am.cpu().numpy(), accept_len=alen.cpu().numpy(), accepted_nodes=anodes.cpu().numpy(),
+                   bonus=bonus.cpu().numpy(), err=binding.sv_get_device_error(ws))
+        _assert_accept_equal(res, ref, case)
+    # keys and tickets are back to zero after the last call
+    assert int(ws[256:].count_nonzero()) == 0
+
+
 def _commit_check(case, paths, alens, layers):
     dc = DeviceCase(case, layers=layers)
     L_ = len(layers)
