@@ -388,6 +388,38 @@ def retrieval_timing(torch, st, args, world):
             "reduce": "mean", "sink_tokens": sink, "window_tokens": window, "topk_pages": topk}
 
 
+def accept_commit_timing(torch, st, args, world, peak):
+    """sv_greedy_accept and sv_kv_commit each timed alone in a CUDA graph.
+    The acceptance rotates copies of the logits so that together they exceed
+    L2 (each call reads its logits from HBM, as in the step)."""
+    c, b = st.case, st.binding
+    logits_bytes = st.logits.numel() * 4
+    copies = int(min(8, max(1, -(-200_000_000 // logits_bytes))))
+    bufs = [st.logits] + [st.logits.clone() for _ in range(copies - 1)]
+
+    def accept_only():
+        for lg in bufs:
+            b.sv_greedy_accept(lg, c.vocab, st.tokens, st.parents, st.cu_nodes, c.batch, st.T, c.max_nodes,
+                               c.max_depth, st.am, st.alen, st.anodes, st.bonus, st.ws_acc)
+
+    def commit_only():
+        b.sv_kv_commit(st.tree_k, st.tree_v, st.T * st.Hkv * st.D, st.k_cache, st.v_cache,
+                       c.num_pages * st.Hkv * c.page_size * st.D, st.layers, c.num_pages, st.block_table,
+                       c.max_pages_per_seq, st.ctx_lens, st.cu_nodes, st.anodes, st.alen, c.batch, c.max_depth,
+                       st.Hkv, st.D, c.page_size, st.new_lens, st.ws)
+
+    ms_a, _ = _time_graph(torch, accept_only, args.steps, args.warmup, world)
+    ms_c, _ = _time_graph(torch, commit_only, args.steps, args.warmup, world)
+    us_a = ms_a * 1e3 / (args.steps * copies)
+    us_c = ms_c * 1e3 / args.steps
+    slots = int(np.sum(np.asarray(c.planted_len) + 1))                      # root + accepted nodes
+    commit_bytes = 2 * slots * 2 * st.Hkv * st.D * 2 * st.layers            # K and V, read + written
+    gbs_a = logits_bytes / (us_a * 1e-6) / 1e9
+    return {"accept_us": us_a, "accept_gbs": gbs_a, "accept_frac": gbs_a / peak,
+            "accept_bytes": logits_bytes, "accept_logits_copies": copies,
+            "commit_us": us_c, "commit_gbs": commit_bytes / (us_c * 1e-6) / 1e9, "commit_bytes": commit_bytes}
+
+
 def run_gpu(args):
     import torch
 
@@ -453,6 +485,7 @@ def run_gpu(args):
     e2e_value = world * nodes_per_step / (ms_e2e * 1e-3 / args.steps)
 
     retrieval = retrieval_timing(torch, st, args, world) if partial else None
+    acc_commit = accept_commit_timing(torch, st, args, world, peak)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -483,6 +516,7 @@ def run_gpu(args):
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": st.launches_per_step() * args.steps,
             "clocks": clocks,
+            "accept_commit": acc_commit,
             **({"retrieval": retrieval} if retrieval else {}),
         }
         print(json.dumps(line), flush=True)

@@ -18,7 +18,8 @@
 //
 // Kernels: page_summary_kernel (one warp per (page, KV head): max/min of the
 // page's valid keys, bf16), query_aggregate_kernel (averaged q+, q- per
-// (sequence, KV head)), page_score_kernel (one warp per page),
+// (sequence, KV head)), page_score_kernel (one warp per page, the
+// sequence's averaged queries staged in shared memory),
 // select_kernel (one CTA per sequence: radix select of the k-th largest
 // importance, ties to the lower page, then the sink, retrieved and window
 // pages written in ascending order).
@@ -100,15 +101,23 @@ __global__ void __launch_bounds__(256) page_summary_kernel(const __grid_constant
     mx[e] = -INFINITY;
     mn[e] = INFINITY;
   }
-  for (int t = 0; t < valid; ++t) {
-    uint32_t v[E / 2];
+  // all sixteen rows are requested before any is used (rows past the valid
+  // tokens repeat row 0, which cannot change a max or a min)
+  uint32_t rows[kPage][E / 2];
+#pragma unroll
+  for (int t = 0; t < kPage; ++t) {
+    const int tt = t < valid ? t : 0;
     if constexpr (E == 4) {
-      const uint2 x = __ldg(reinterpret_cast<const uint2*>(src + t * D));
-      v[0] = x.x;
-      v[1] = x.y;
+      const uint2 x = __ldg(reinterpret_cast<const uint2*>(src + tt * D));
+      rows[t][0] = x.x;
+      rows[t][1] = x.y;
     } else {
-      v[0] = __ldg(reinterpret_cast<const unsigned int*>(src + t * D));
+      rows[t][0] = __ldg(reinterpret_cast<const unsigned int*>(src + tt * D));
     }
+  }
+#pragma unroll
+  for (int t = 0; t < kPage; ++t) {
+    const uint32_t* v = rows[t];
 #pragma unroll
     for (int e = 0; e < E / 2; ++e) {
       const float lo = __uint_as_float(v[e] << 16), hi = __uint_as_float(v[e] & 0xFFFF0000u);
@@ -148,41 +157,68 @@ struct AggParams {
 
 // The mean over the used queries of q+ and q-, split by KV head: the sum
 // over KV heads of qa . (kmax, kmin) is then the mean score.  One CTA per
-// (KV head, sequence): 1024 threads, D per row slice, each slice summing
-// every R-th query row of the group before a shared-memory reduction.
+// (KV head, sequence), 1024 threads: a thread owns eight dimensions of every
+// (1024 / (D / 8))-th query row and requests all its rows with 16-byte loads
+// before summing them, so the whole group arrives in one round trip; the
+// row slices are then folded within each warp by shuffles and across warps
+// in shared memory (a fixed order: the result does not depend on timing).
 template <int D>
 __global__ void __launch_bounds__(1024) query_aggregate_kernel(const __grid_constant__ AggParams p) {
-  constexpr int R = 1024 / D;  // row slices
-  __shared__ float red[2][R][D];
+  constexpr int kChunks = D / 8;             // 16-byte chunks of a row
+  constexpr int kSlices = 1024 / kChunks;    // row slices
+  constexpr int kWarpSlices = 32 / kChunks;  // slices inside one warp
+  __shared__ float red[2][32][D];
   const int kvh = blockIdx.x;
   const int b = blockIdx.y;
-  const int d = threadIdx.x % D;
-  const int slice = threadIdx.x / D;
+  const int c = threadIdx.x % kChunks;
+  const int slice = threadIdx.x / kChunks;
   const int n0 = p.cu_nodes[b];
   const int N = p.cu_nodes[b + 1] - n0;
   const int i0 = p.last_only ? max(0, N - 1) : 0;
   const int used = N - i0;
   const int rows = used * p.group;
-  float pos = 0.f, neg = 0.f;
-#pragma unroll 4
-  for (int r = slice; r < rows; r += R) {
+  float pos[8], neg[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) pos[e] = neg[e] = 0.f;
+#pragma unroll 8
+  for (int r = slice; r < rows; r += kSlices) {
     const int i = i0 + r / p.group, g = r % p.group;
-    const float v = __bfloat162float(p.q[(static_cast<size_t>(n0 + i) * p.num_q_heads + kvh * p.group + g) * D + d]);
-    pos += fmaxf(v, 0.f);
-    neg += fminf(v, 0.f);
-  }
-  red[0][slice][d] = pos;
-  red[1][slice][d] = neg;
-  __syncthreads();
-  if (slice == 0) {
-    for (int s2 = 1; s2 < R; ++s2) {
-      pos += red[0][s2][d];
-      neg += red[1][s2][d];
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+        p.q + (static_cast<size_t>(n0 + i) * p.num_q_heads + kvh * p.group + g) * D + c * 8));
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xFFFF0000u);
+      pos[2 * e] += fmaxf(lo, 0.f);
+      neg[2 * e] += fminf(lo, 0.f);
+      pos[2 * e + 1] += fmaxf(hi, 0.f);
+      neg[2 * e + 1] += fminf(hi, 0.f);
     }
+  }
+  // slices of one warp: lanes c, c + kChunks, ... hold the same dimensions
+#pragma unroll
+  for (int o = kChunks; o < 32; o <<= 1)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      pos[e] += __shfl_xor_sync(0xffffffffu, pos[e], o);
+      neg[e] += __shfl_xor_sync(0xffffffffu, neg[e], o);
+    }
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) < kChunks) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      red[0][warp][c * 8 + e] = pos[e];
+      red[1][warp][c * 8 + e] = neg[e];
+    }
+  }
+  __syncthreads();
+  static_assert(kWarpSlices >= 1 && 2 * D <= 1024, "row slices");
+  if (threadIdx.x < 2 * D) {
+    const int half = threadIdx.x / D, d = threadIdx.x % D;
+    float acc = 0.f;
+    for (int w = 0; w < 32; ++w) acc += red[half][w][d];
     const float scale = used > 0 ? 1.f / (static_cast<float>(used) * p.num_q_heads) : 0.f;
-    float* dst = p.qa + (static_cast<size_t>(b) * gridDim.x + kvh) * 2 * D + d;
-    dst[0] = pos * scale;
-    dst[D] = neg * scale;
+    p.qa[(static_cast<size_t>(b) * gridDim.x + kvh) * 2 * D + half * D + d] = acc * scale;
   }
 }
 
@@ -211,9 +247,18 @@ struct ScoreParams {
 template <int D>
 __global__ void __launch_bounds__(256) page_score_kernel(const __grid_constant__ ScoreParams p) {
   constexpr int E = D / 32;
+  extern __shared__ float qa_s[];  // mean / last: this sequence's qa, [Hkv][2][D]
   const int b = blockIdx.y;
   const int lp = blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  if (!p.reduce_max) {
+    // every warp of the CTA scores a page of this sequence against the same
+    // averaged queries: read them once per CTA
+    const float4* src = reinterpret_cast<const float4*>(p.qa + static_cast<size_t>(b) * p.num_kv_heads * 2 * D);
+    float4* dst = reinterpret_cast<float4*>(qa_s);
+    for (int i = threadIdx.x; i < p.num_kv_heads * 2 * D / 4; i += blockDim.x) dst[i] = src[i];
+    __syncthreads();
+  }
   if (lp >= p.max_ctx_pages) return;
   const int L = clamp_len(p.ctx_lens[b], p.max_ctx_pages);
   const Regions rg = regions(L, p.sink_tokens, p.window_tokens);
@@ -228,11 +273,27 @@ __global__ void __launch_bounds__(256) page_score_kernel(const __grid_constant__
       float acc = 0.f;
 #pragma unroll 8
       for (int kvh = 0; kvh < p.num_kv_heads; ++kvh) {
+        // this lane's E maxima and E minima (bf16, one 4- or 8-byte load each)
         const __nv_bfloat16* s = p.summ + (static_cast<size_t>(phys) * p.num_kv_heads + kvh) * 2 * D + lane * E;
-        const float* a = p.qa + (static_cast<size_t>(b) * p.num_kv_heads + kvh) * 2 * D + lane * E;
+        uint32_t mx[E / 2], mn[E / 2];
+        if constexpr (E == 4) {
+          const uint2 a2 = __ldg(reinterpret_cast<const uint2*>(s));
+          const uint2 b2 = __ldg(reinterpret_cast<const uint2*>(s + D));
+          mx[0] = a2.x;
+          mx[1] = a2.y;
+          mn[0] = b2.x;
+          mn[1] = b2.y;
+        } else {
+          mx[0] = __ldg(reinterpret_cast<const unsigned int*>(s));
+          mn[0] = __ldg(reinterpret_cast<const unsigned int*>(s + D));
+        }
+        const float* a = qa_s + kvh * 2 * D + lane * E;
 #pragma unroll
-        for (int e = 0; e < E; ++e)
-          acc += a[e] * __bfloat162float(s[e]) + a[D + e] * __bfloat162float(s[D + e]);
+        for (int e = 0; e < E / 2; ++e) {
+          acc += a[2 * e] * __uint_as_float(mx[e] << 16) + a[2 * e + 1] * __uint_as_float(mx[e] & 0xFFFF0000u);
+          acc += a[D + 2 * e] * __uint_as_float(mn[e] << 16) +
+                 a[D + 2 * e + 1] * __uint_as_float(mn[e] & 0xFFFF0000u);
+        }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
@@ -361,9 +422,15 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const __grid_consta
   for (int shift = 24; shift >= 0 && k > 0; shift -= 8) {
     for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0;
     __syncthreads();
-    for (int i = tid; i < ncand; i += kSelThreads) {
-      const uint32_t c = code[i];
-      if ((c & mask) == prefix) atomicAdd(&hist[(c >> shift) & 255u], 1);
+    // Scores of one sequence share their high bits, so most codes fall into
+    // a few bins: lanes holding the same digit add once, as a group.
+    for (int base = 0; base < ncand; base += kSelThreads) {
+      const int i = base + tid;
+      const uint32_t c = i < ncand ? code[i] : 0u;
+      const bool part = i < ncand && (c & mask) == prefix;
+      const uint32_t key = part ? (c >> shift) & 255u : 0xFFFFFFFFu;
+      const uint32_t peers = __match_any_sync(0xffffffffu, key);
+      if (part && (tid & 31) == __ffs(peers) - 1) atomicAdd(&hist[key], __popc(peers));
     }
     __syncthreads();
     if (tid < 32) {
@@ -593,6 +660,8 @@ sv_status sv_retrieve_pages(const sv_retrieve_params* rp, sv_stream_t stream) {
   if (r.head_dim != 64 && r.head_dim != 128) return SV_ERR_UNSUPPORTED;
   if (r.page_size != retr::kPage) return SV_ERR_UNSUPPORTED;
   if (r.max_ctx_pages > retr::kMaxSortPages || r.max_ctx_pages > r.max_pages_per_seq) return SV_ERR_UNSUPPORTED;
+  if (static_cast<size_t>(r.num_kv_heads) * 2 * r.head_dim * sizeof(float) > 227 * 1024)
+    return SV_ERR_UNSUPPORTED;  // the averaged queries of a sequence must fit in shared memory
   if (!aligned16(r.q) || !aligned16(r.summaries)) return SV_ERR_INVALID_ARG;
   const long long per_seq =
       (r.sink_tokens + retr::kPage - 1) / retr::kPage + static_cast<long long>(r.topk) +
@@ -648,8 +717,19 @@ sv_status sv_retrieve_pages(const sv_retrieve_params* rp, sv_stream_t stream) {
     sp.window_tokens = r.window_tokens;
     sp.reduce_max = use_max ? 1 : 0;
     const dim3 grid((r.max_ctx_pages + retr::kWarpsPerCta - 1) / retr::kWarpsPerCta, r.batch, 1);
-    if (r.head_dim == 128) retr::page_score_kernel<128><<<grid, 256, 0, s>>>(sp);
-    else retr::page_score_kernel<64><<<grid, 256, 0, s>>>(sp);
+    const size_t qa_smem = use_max ? 0 : static_cast<size_t>(r.num_kv_heads) * 2 * r.head_dim * sizeof(float);
+    if (qa_smem > 48 * 1024) {
+      const cudaError_t e = r.head_dim == 128
+                                ? cudaFuncSetAttribute(retr::page_score_kernel<128>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       static_cast<int>(qa_smem))
+                                : cudaFuncSetAttribute(retr::page_score_kernel<64>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       static_cast<int>(qa_smem));
+      if (e != cudaSuccess) return SV_ERR_CUDA;
+    }
+    if (r.head_dim == 128) retr::page_score_kernel<128><<<grid, 256, qa_smem, s>>>(sp);
+    else retr::page_score_kernel<64><<<grid, 256, qa_smem, s>>>(sp);
     if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
   }
   retr::SelParams sel;
