@@ -12,6 +12,8 @@ verification hot path computes, written from the method descriptions:
   L .. L + a.
 * ``retrieval``  — SpecPV block retrieval: max/min key summaries of 16-token
   pages, block importance against the tree's queries, the partial page list.
+* ``sampling``   — stochastic (temperature > 0) acceptance: speculative
+  sampling node by node over the tree, residual draws for the bonus token.
 
 Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU
 baseline leg may import this package.  The CUDA library never calls it and
@@ -19,7 +21,8 @@ shares no code with it.
 
 Pins: every function here is checked in ``tests/test_oracle_*.py`` against
 library routines, closed forms, invariants, the SpecBlock Appendix A.2 mask
-example and brute force.  Nothing here is "parity unpinned".
+example, brute force and (for sampling) the distribution speculative sampling
+must reproduce.  Nothing here is "parity unpinned".
 """
 
 from .attention import (  # noqa: F401
@@ -31,6 +34,7 @@ from .attention import (  # noqa: F401
 )
 from .accept import greedy_accept  # noqa: F401
 from .commit import kv_commit  # noqa: F401
+from .sampling import inverse_cdf, node_verify, speculative_tree_accept, target_probs  # noqa: F401
 from .retrieval import (  # noqa: F401
     extend_partial_lists,
     specpv_schedule,
