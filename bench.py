@@ -389,9 +389,10 @@ def retrieval_timing(torch, st, args, world):
 
 
 def accept_commit_timing(torch, st, args, world, peak):
-    """sv_greedy_accept and sv_kv_commit each timed alone in a CUDA graph.
-    The acceptance rotates copies of the logits so that together they exceed
-    L2 (each call reads its logits from HBM, as in the step)."""
+    """sv_greedy_accept, sv_kv_commit and sv_sample_accept (temperature 1)
+    each timed alone in a CUDA graph.  The acceptances rotate copies of the
+    logits (and of the drafts) so that together they exceed L2: each call
+    reads its inputs from HBM, as in the step."""
     c, b = st.case, st.binding
     logits_bytes = st.logits.numel() * 4
     copies = int(min(8, max(1, -(-200_000_000 // logits_bytes))))
@@ -408,16 +409,36 @@ def accept_commit_timing(torch, st, args, world, peak):
                        c.max_pages_per_seq, st.ctx_lens, st.cu_nodes, st.anodes, st.alen, c.batch, c.max_depth,
                        st.Hkv, st.D, c.page_size, st.new_lens, st.ws)
 
+    # stochastic acceptance at temperature 1 (drafts near the target), on
+    # the same logits copies and one draft array per copy
+    from synth import make_sampling_inputs
+    q_np, tok_np, ua_np, ub_np = make_sampling_inputs(c, seed=1)
+    qs = [torch.from_numpy(q_np).to(st.dev)] + [None] * (copies - 1)
+    for i in range(1, copies):
+        qs[i] = qs[0].clone()
+    s_tok = torch.from_numpy(tok_np).to(st.dev)
+    s_ua, s_ub = torch.from_numpy(ua_np).to(st.dev), torch.from_numpy(ub_np).to(st.dev)
+    s_ws = torch.zeros(b.sv_sample_accept_workspace_size(c.batch, st.T), dtype=torch.uint8, device=st.dev)
+
+    def sample_only():
+        for lg, qq in zip(bufs, qs):
+            b.sv_sample_accept(lg, qq, c.vocab, 1.0, s_tok, st.parents, st.cu_nodes, c.batch, st.T, c.max_nodes,
+                               c.max_depth, s_ua, s_ub, None, st.alen, st.anodes, st.bonus, s_ws)
+
     ms_a, _ = _time_graph(torch, accept_only, args.steps, args.warmup, world)
     ms_c, _ = _time_graph(torch, commit_only, args.steps, args.warmup, world)
+    ms_s, _ = _time_graph(torch, sample_only, args.steps, args.warmup, world)
     us_a = ms_a * 1e3 / (args.steps * copies)
     us_c = ms_c * 1e3 / args.steps
+    us_s = ms_s * 1e3 / (args.steps * copies)
     slots = int(np.sum(np.asarray(c.planted_len) + 1))                      # root + accepted nodes
     commit_bytes = 2 * slots * 2 * st.Hkv * st.D * 2 * st.layers            # K and V, read + written
     gbs_a = logits_bytes / (us_a * 1e-6) / 1e9
     return {"accept_us": us_a, "accept_gbs": gbs_a, "accept_frac": gbs_a / peak,
             "accept_bytes": logits_bytes, "accept_logits_copies": copies,
-            "commit_us": us_c, "commit_gbs": commit_bytes / (us_c * 1e-6) / 1e9, "commit_bytes": commit_bytes}
+            "commit_us": us_c, "commit_gbs": commit_bytes / (us_c * 1e-6) / 1e9, "commit_bytes": commit_bytes,
+            "sample_accept_us": us_s, "sample_accept_gbs": 2 * logits_bytes / (us_s * 1e-6) / 1e9,
+            "sample_accept_bytes": 2 * logits_bytes, "sample_temperature": 1.0}
 
 
 def run_gpu(args):

@@ -12,6 +12,7 @@
  *                      partial page list), one layer per call;
  *   sv_greedy_accept   per-node vocabulary arg-max and the longest accepted
  *                      root path (temperature 0);
+ *   sv_sample_accept   speculative sampling over the tree (temperature > 0);
  *   sv_kv_commit       copy of the accepted path's K/V into the paged cache
  *                      for every layer.
  *
@@ -234,6 +235,48 @@ sv_status sv_greedy_accept_noalloc(const float* logits, int vocab, const int* to
                                    int total_nodes, int max_nodes, int max_depth,
                                    int* argmax_out, int* accept_len, int* accepted_nodes,
                                    int* bonus_token, int* device_error, sv_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Stochastic (temperature > 0) acceptance of a verified draft tree.
+ *
+ * Defined by: speculative sampling (SpecPV section 2, citing Leviathan et
+ * al.: the emitted tokens follow the target's own sampling distribution) over
+ * a token tree (SpecPV section 2, SpecInfer), at the temperatures SpecBlock
+ * section 4 and SpecPV Appendix E evaluate.  The pages give no rule for a
+ * tree; this follows SpecInfer's multi-step speculative sampling:
+ *   p_u = softmax(logits[u] / temperature); the children c of node u (drawn
+ *   from draft_probs[u]) are tried in index order against a residual R that
+ *   starts as p_u: c (token x) is accepted when u_accept[c] < min(1, R(x) /
+ *   q_u(x)) (q_u(x) = 0 accepts); otherwise R <- max(R - q_u, 0) / its sum
+ *   (unchanged when the sum is 0).  From the root the walk follows accepted
+ *   children to a node z; accept_len is its depth, accepted_nodes its root
+ *   path, and bonus_token the smallest x with R_z(0) + ... + R_z(x) >
+ *   u_bonus[z] * sum(R_z), R_z being z's residual after all its children
+ *   were rejected (p_z for a leaf).
+ *
+ *   logits       fp32 [total_nodes, vocab], the target's logits per node
+ *   draft_probs  fp32 [total_nodes, vocab], per node the probability vector
+ *                its children were drawn from (rows of leaves are read only
+ *                if the walk ends there and then not at all)
+ *   u_accept     fp32 [total_nodes], uniform in [0, 1): node n's test at its
+ *                parent (the root's is unused)
+ *   u_bonus      fp32 [total_nodes], uniform in [0, 1): the draw at node n
+ *   accepted_child (optional) int32 [total_nodes]: per node the local index
+ *                of its accepted child, -1 if none
+ *   accept_len, accepted_nodes, bonus_token: as for sv_greedy_accept.
+ * vocab >= 8 and <= 2^24; temperature > 0 and finite; max_nodes <= 128.
+ * The workspace (sv_sample_accept_workspace_size bytes) holds per-node
+ * scalars between the two launches; it needs no zeroing between calls.
+ * ---------------------------------------------------------------------- */
+sv_status sv_sample_accept_workspace_size(int batch, int total_nodes, size_t* bytes);
+
+sv_status sv_sample_accept(const float* logits, const float* draft_probs, int vocab,
+                           float temperature, const int* tokens, const int* parents,
+                           const int* cu_nodes, int batch, int total_nodes, int max_nodes,
+                           int max_depth, const float* u_accept, const float* u_bonus,
+                           int* accepted_child, int* accept_len, int* accepted_nodes,
+                           int* bonus_token, void* workspace, size_t workspace_bytes,
+                           sv_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * KV commit of the accepted path, all layers in one launch.

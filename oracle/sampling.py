@@ -92,17 +92,25 @@ def speculative_tree_accept(logits, draft_probs, tokens, parents, cu_nodes, temp
       ``accept_len``     int64 [B]
       ``accepted_nodes`` list of B lists of local node ids, root first
       ``bonus``          int64 [B]
-      ``margin``         float64 [B]: the smallest decision margin on the
-                         sequence's walk (acceptance tests made at the nodes
-                         of the path, and the bonus draw)
+      ``walk_margin``    float64 [B]: the smallest margin of the acceptance
+                         tests made at the nodes of the walk
+      ``bonus_margin``   float64 [B]: the distance of the bonus uniform from
+                         the cumulative sums around the drawn token
+      ``node_margin``    float64 [T]: per node the smallest margin of its
+                         acceptance tests (inf for leaves)
+      ``residual_z``     list of B float64 arrays: the distribution the bonus
+                         was drawn from
     """
     logits = np.asarray(logits)
     T = logits.shape[0]
     B = len(cu_nodes) - 1
     acc_child = np.full(T, -1, dtype=np.int64)
+    node_margin = np.full(T, np.inf)
     acc_len = np.zeros(B, dtype=np.int64)
     bonus = np.zeros(B, dtype=np.int64)
-    margin = np.full(B, np.inf)
+    walk_margin = np.full(B, np.inf)
+    bonus_margin = np.full(B, np.inf)
+    residual_z = []
     paths: List[List[int]] = []
     for b in range(B):
         n0, n1 = int(cu_nodes[b]), int(cu_nodes[b + 1])
@@ -123,6 +131,7 @@ def speculative_tree_accept(logits, draft_probs, tokens, parents, cu_nodes, temp
                 acc_child[n0 + u] = children[u][i]
             residual[u] = R
             node_margins[u] = m
+            node_margin[n0 + u] = min(m)
         z = 0
         path = [0]
         mg = np.inf
@@ -141,5 +150,8 @@ def speculative_tree_accept(logits, draft_probs, tokens, parents, cu_nodes, temp
         paths.append(path)
         acc_len[b] = len(path) - 1
         bonus[b] = x
-        margin[b] = min(mg, m)
-    return dict(accepted_child=acc_child, accept_len=acc_len, accepted_nodes=paths, bonus=bonus, margin=margin)
+        walk_margin[b] = mg
+        bonus_margin[b] = m
+        residual_z.append(R)
+    return dict(accepted_child=acc_child, accept_len=acc_len, accepted_nodes=paths, bonus=bonus,
+                walk_margin=walk_margin, bonus_margin=bonus_margin, node_margin=node_margin, residual_z=residual_z)

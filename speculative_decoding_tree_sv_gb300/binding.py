@@ -98,6 +98,12 @@ def load(path: Optional[str] = None):
     lib.sv_greedy_accept_noalloc.restype = c_int
     lib.sv_greedy_accept_noalloc.argtypes = [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
                                              c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+    lib.sv_sample_accept_workspace_size.restype = c_int
+    lib.sv_sample_accept_workspace_size.argtypes = [c_int, c_int, P(c_size_t)]
+    lib.sv_sample_accept.restype = c_int
+    lib.sv_sample_accept.argtypes = [c_void_p, c_void_p, c_int, ctypes.c_float, c_void_p, c_void_p, c_void_p,
+                                     c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
+                                     c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
     lib.sv_kv_commit.restype = c_int
     lib.sv_kv_commit.argtypes = [c_void_p, c_void_p, c_longlong, c_void_p, c_void_p, c_longlong, c_int, c_int,
                                  c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
@@ -239,6 +245,28 @@ def sv_greedy_accept_noalloc(logits, vocab: int, tokens, parents, cu_nodes, batc
                                            batch, total_nodes, max_nodes, max_depth, _ptr(argmax_out),
                                            _ptr(accept_len), _ptr(accepted_nodes), _ptr(bonus_token),
                                            _ptr(device_error), _stream(stream)), "sv_greedy_accept_noalloc")
+
+
+def sv_sample_accept_workspace_size(batch: int, total_nodes: int) -> int:
+    n = c_size_t(0)
+    _check(load().sv_sample_accept_workspace_size(batch, total_nodes, ctypes.byref(n)),
+           "sv_sample_accept_workspace_size")
+    return int(n.value)
+
+
+def sv_sample_accept(logits, draft_probs, vocab: int, temperature: float, tokens, parents, cu_nodes, batch: int,
+                     total_nodes: int, max_nodes: int, max_depth: int, u_accept, u_bonus, accepted_child,
+                     accept_len, accepted_nodes, bonus_token, workspace, workspace_bytes: Optional[int] = None,
+                     stream=None) -> None:
+    """Stochastic (temperature > 0) acceptance: speculative sampling node by
+    node over the tree (see include/sv.h for the rule and the layouts)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(load().sv_sample_accept(_ptr(logits), _ptr(draft_probs), vocab, float(temperature), _ptr(tokens),
+                                   _ptr(parents), _ptr(cu_nodes), batch, total_nodes, max_nodes, max_depth,
+                                   _ptr(u_accept), _ptr(u_bonus), _ptr(accepted_child), _ptr(accept_len),
+                                   _ptr(accepted_nodes), _ptr(bonus_token), _ptr(workspace), workspace_bytes,
+                                   _stream(stream)), "sv_sample_accept")
 
 
 def sv_kv_commit(tree_k, tree_v, tree_layer_stride: int, k_cache, v_cache, cache_layer_stride: int,

@@ -449,3 +449,38 @@ def _plant_logits(case: VerifyCase, r_logit, r_plant, plant, depths, parents_lis
     case.planted_len = plens
     case.planted_path = paths
     case.planted_bonus = bonus
+
+
+def make_sampling_inputs(case: VerifyCase, *, seed: int = 0, sharpness: float = 1.0, closeness: float = 0.5,
+                         draft: str = "near"):
+    """Inputs of stochastic acceptance for a case that has logits: per node a
+    draft probability vector (float32 [T, V], each row sums to 1), children
+    tokens redrawn independently from their parent's draft row, and two
+    uniforms per node in [0, 1).
+
+    draft "near": rows proportional to exp(sharpness * (logits + noise)), the
+    noise N(0, closeness) so that drafts resemble the target; "flat": uniform
+    rows.  The case's tokens are replaced (int32 [T]); the root's stays 0."""
+    assert case.logits is not None
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 0x5A3]))
+    T, V = case.logits.shape
+    if draft == "flat":
+        q = np.full((T, V), 1.0 / V, dtype=np.float64)
+    else:
+        z = sharpness * (case.logits.astype(np.float64) + rng.normal(0.0, closeness, size=(T, V)))
+        z -= z.max(axis=1, keepdims=True)
+        q = np.exp(z)
+        q /= q.sum(axis=1, keepdims=True)
+    q32 = q.astype(np.float32)
+    q32 /= q32.sum(axis=1, keepdims=True, dtype=np.float64).astype(np.float32)
+    tokens = np.zeros(T, dtype=np.int32)
+    cdf = None
+    for b in range(case.batch):
+        n0, n1 = int(case.cu_nodes[b]), int(case.cu_nodes[b + 1])
+        for c in range(n0 + 1, n1):
+            par = n0 + int(case.parents[c])
+            cdf = np.cumsum(q[par])
+            tokens[c] = min(V - 1, int(np.searchsorted(cdf, rng.random() * cdf[-1], side="right")))
+    u_accept = rng.random(T).astype(np.float32)
+    u_bonus = rng.random(T).astype(np.float32)
+    return q32, tokens, u_accept, u_bonus

@@ -109,6 +109,33 @@ def test_accept_host_validation(lib):
     assert f(a, 0, a, a, a, 1, 4, 4, 3, None, a, a, a, a, need, None) == 1
 
 
+def test_sample_accept_host_validation(lib):
+    a = 1 << 20
+    need = binding.sv_sample_accept_workspace_size(4, 100)
+    assert need >= 256 + 100 * 4 * 2 + 100 * 129 * 4
+    f = lib.sv_sample_accept
+
+    def call(**kw):
+        args = dict(logits=a, q=a, vocab=1000, temp=1.0, tokens=a, parents=a, cu=a, batch=4, total=100,
+                    max_nodes=60, max_depth=8, ua=a, ub=a, acc=None, alen=a, anodes=a, bonus=a, ws=a,
+                    ws_bytes=need)
+        args.update(kw)
+        return f(*args.values(), None)
+
+    assert call(logits=None) == 1
+    assert call(q=None) == 1
+    assert call(ua=None) == 1
+    assert call(temp=0.0) == 1                        # temperature must be positive
+    assert call(temp=-1.0) == 1
+    assert call(temp=float("inf")) == 1
+    assert call(temp=float("nan")) == 1
+    assert call(vocab=4) == 1                         # below one entry per CTA of a cluster
+    assert call(max_nodes=129) == 2
+    assert call(vocab=(1 << 24) + 1) == 2
+    assert call(ws_bytes=need - 1) == 4
+    assert call(total=0) == 0                         # nothing to do, nothing launched
+
+
 def test_commit_host_validation(lib):
     a = 1 << 20
     f = lib.sv_kv_commit
