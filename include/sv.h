@@ -456,9 +456,20 @@ typedef enum sv_trace_event {
 sv_status sv_set_trace_buffer(void* buffer, size_t bytes);
 
 /* Reads the error word of a workspace (waits for `stream`), stores it in
- * *code (host) and resets it to zero.  Returns SV_ERR_DEVICE if it was
- * nonzero, SV_OK otherwise. */
+ * *code (host) and resets it to zero.  Returns SV_ERR_TIMEOUT if it held
+ * SV_DEVERR_TIMEOUT, SV_ERR_DEVICE for any other nonzero code, SV_OK
+ * otherwise. */
 sv_status sv_get_device_error(void* workspace, int* code, sv_stream_t stream);
+
+/* Diagnostics: exercises the bounded wait every kernel of this library uses
+ * on its mbarriers.  Launches one CTA that waits for a barrier nothing will
+ * complete.  With abort_after_ns == 0 the wait gives up after the library's
+ * limit (2 s); with 0 < abort_after_ns < 2e9 another warp of the CTA raises
+ * the abort flag after that long, as a failing role of a kernel does.  Either
+ * way the kernel records SV_DEVERR_TIMEOUT in the error word of `workspace`
+ * (a device int, zero before the call) and returns; the context stays
+ * usable.  Read the outcome with sv_get_device_error. */
+sv_status sv_selftest_bounded_wait(void* workspace, long long abort_after_ns, sv_stream_t stream);
 
 #ifdef __cplusplus
 }  /* extern "C" */

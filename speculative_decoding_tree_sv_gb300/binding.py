@@ -20,6 +20,9 @@ from . import build as _build
 SV_OK = 0
 STATUS_NAMES = {0: "SV_OK", 1: "SV_ERR_INVALID_ARG", 2: "SV_ERR_UNSUPPORTED", 3: "SV_ERR_CUDA",
                 4: "SV_ERR_WORKSPACE", 5: "SV_ERR_DEVICE", 6: "SV_ERR_TIMEOUT"}
+# device error codes (sv_deverr in include/sv.h)
+SV_DEVERR_NONE, SV_DEVERR_TIMEOUT, SV_DEVERR_BAD_PARENT, SV_DEVERR_BAD_PAGE = 0, 1, 2, 3
+SV_DEVERR_BAD_PATH, SV_DEVERR_DEPTH, SV_DEVERR_BAD_TREE = 4, 5, 6
 SV_ATTN_EARLY_CONTEXT = 1
 SV_ATTN_KERNEL_PAIRED = 2
 SV_ATTN_KERNEL_WIDE = 4
@@ -104,6 +107,8 @@ def load(path: Optional[str] = None):
     lib.sv_sample_accept.argtypes = [c_void_p, c_void_p, c_int, ctypes.c_float, c_void_p, c_void_p, c_void_p,
                                      c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p, c_void_p,
                                      c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
+    lib.sv_selftest_bounded_wait.restype = c_int
+    lib.sv_selftest_bounded_wait.argtypes = [c_void_p, c_longlong, c_void_p]
     lib.sv_kv_commit.restype = c_int
     lib.sv_kv_commit.argtypes = [c_void_p, c_void_p, c_longlong, c_void_p, c_void_p, c_longlong, c_int, c_int,
                                  c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
@@ -245,6 +250,13 @@ def sv_greedy_accept_noalloc(logits, vocab: int, tokens, parents, cu_nodes, batc
                                            batch, total_nodes, max_nodes, max_depth, _ptr(argmax_out),
                                            _ptr(accept_len), _ptr(accepted_nodes), _ptr(bonus_token),
                                            _ptr(device_error), _stream(stream)), "sv_greedy_accept_noalloc")
+
+
+def sv_selftest_bounded_wait(workspace, abort_after_ns: int = 0, stream=None) -> None:
+    """Launches a kernel whose bounded mbarrier wait must give up (see
+    include/sv.h); read the outcome with sv_get_device_error."""
+    _check(load().sv_selftest_bounded_wait(_ptr(workspace), int(abort_after_ns), _stream(stream)),
+           "sv_selftest_bounded_wait")
 
 
 def sv_sample_accept_workspace_size(batch: int, total_nodes: int) -> int:

@@ -1,7 +1,9 @@
 // Host-side common entry points: version, status names, the device error
-// word, driver entry-point resolution for tensor maps, SM count.
+// word, driver entry-point resolution for tensor maps, SM count; and a
+// self-test of the bounded device wait.
 #include <mutex>
 
+#include "sv_device.cuh"
 #include "sv_internal.h"
 
 namespace sv {
@@ -52,11 +54,44 @@ int device_sm_count() {
   return n;
 }
 
+// A wait that can never complete: one CTA initialises an mbarrier that
+// nothing arrives on and waits for its first phase with the bounded wait
+// every kernel of the library uses.  With `abort_after_ns` > 0 a second warp
+// raises the shared abort flag after that long instead, the way a role of a
+// kernel stops the others.  Either way the wait gives up, SV_DEVERR_TIMEOUT
+// is recorded and the kernel returns normally.
+__global__ void __launch_bounds__(64) bounded_wait_selftest_kernel(int* err, unsigned long long abort_after_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (!mbar_wait(&bar, 0, &abort_flag)) report_error(err, SV_DEVERR_TIMEOUT);
+  } else if (threadIdx.x == 32 && abort_after_ns > 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < abort_after_ns) {
+    }
+    *reinterpret_cast<volatile int*>(&abort_flag) = 1;
+  }
+}
+
 }  // namespace sv
 
 extern "C" {
 
 int sv_abi_version(void) { return 2; }
+
+sv_status sv_selftest_bounded_wait(void* workspace, long long abort_after_ns, sv_stream_t stream) {
+  if (workspace == nullptr || abort_after_ns < 0 || abort_after_ns >= static_cast<long long>(sv::kWaitTimeoutNs))
+    return SV_ERR_INVALID_ARG;
+  sv::bounded_wait_selftest_kernel<<<1, 64, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<int*>(workspace), static_cast<unsigned long long>(abort_after_ns));
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
 
 const char* sv_status_string(sv_status status) {
   switch (status) {

@@ -136,6 +136,13 @@ def test_sample_accept_host_validation(lib):
     assert call(total=0) == 0                         # nothing to do, nothing launched
 
 
+def test_selftest_host_validation(lib):
+    f = lib.sv_selftest_bounded_wait
+    assert f(None, 0, None) == 1
+    assert f(1 << 20, -1, None) == 1
+    assert f(1 << 20, 2_000_000_000, None) == 1       # must abort before the wait's own limit
+
+
 def test_commit_host_validation(lib):
     a = 1 << 20
     f = lib.sv_kv_commit
