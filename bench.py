@@ -467,6 +467,19 @@ def run_gpu(args):
         # attention alone (the dominant kernel) for the roofline
         ms_attn, _ga = _time_graph(torch, st.attention_all_layers, args.steps, args.warmup, world)
     clocks = clk.summary()
+    # the same attention calls without the graph (eager launches, events on
+    # the current stream), for comparison
+    for _ in range(args.warmup):
+        st.attention_all_layers()
+    torch.cuda.synchronize()
+    eager_steps = max(1, min(args.steps, 200))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(eager_steps):
+        st.attention_all_layers()
+    e1.record()
+    torch.cuda.synchronize()
+    attn_eager_us = e0.elapsed_time(e1) * 1e3 / (eager_steps * c.num_layers)
     ms_step = ms / args.steps
     value = world * nodes_per_step / (ms_step * 1e-3)
 
@@ -532,7 +545,8 @@ def run_gpu(args):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
                          "kernel": "sv_tree_attention (attention + split combine)",
-                         "bytes_per_launch": bytes_launch, "launch_us": attn_launch_s * 1e6},
+                         "bytes_per_launch": bytes_launch, "launch_us": attn_launch_s * 1e6,
+                         "launch_us_without_graph": attn_eager_us},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": st.launches_per_step() * args.steps,

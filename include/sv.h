@@ -447,8 +447,8 @@ typedef enum sv_trace_event {
   SV_TRACE_LOOP_END = 6,      /* softmax (row tile 0): last P handed over      */
   SV_TRACE_O_READY = 7,       /* softmax (row tile 0): final O complete        */
   SV_TRACE_EPILOGUE = 8,      /* output or partial written / parked            */
-  SV_TRACE_MERGE_READY = 9,   /* on-chip merge: all peers published            */
-  SV_TRACE_MERGE_DONE = 10,   /* on-chip merge: own rows merged                */
+  SV_TRACE_MERGE_READY = 9,   /* reserved (no current kernel records it)       */
+  SV_TRACE_MERGE_DONE = 10,   /* reserved (no current kernel records it)       */
   SV_TRACE_EXIT = 11,         /* before TMEM release                           */
   SV_TRACE_TREE_MASK = 12     /* softmax (row tile 0): ancestor masks built    */
 } sv_trace_event;
