@@ -140,3 +140,27 @@ def test_workspace_reused_without_clearing():
     q2, tokens2, ua2, ub2 = make_sampling_inputs(case, seed=12)
     second = _run(case, q2, tokens2, ua2, ub2, 1.0, ws=first["ws"])
     _compare(case, second, _oracle(case, q2, tokens2, ua2, ub2, 1.0), ub2)
+
+
+def test_bad_inputs_are_reported_not_trapped():
+    # a walk deeper than max_depth, and a child token outside the vocabulary:
+    # both are recorded in the error word; the call still returns
+    case = make_case("tiny", batch=2)
+    q = np.full((case.total_nodes, case.vocab), 1.0 / case.vocab, dtype=np.float32)
+    ua = np.zeros(case.total_nodes, np.float32)        # every test passes (flat draft, r = 0)
+    ub = np.full(case.total_nodes, 0.5, np.float32)
+    tokens = np.zeros(case.total_nodes, np.int32)
+    res = _run(case, q, tokens, ua, ub, 1.0)
+    assert res["err"] == 0
+    deep = int(res["accept_len"].max())
+    assert deep >= 1
+    # the same inputs with max_depth below the walk's depth
+    short = make_case("tiny", batch=2)
+    short.max_depth = deep - 1
+    res = _run(short, q, tokens, ua, ub, 1.0)
+    assert res["err"] == binding.SV_DEVERR_DEPTH
+    # a token outside [0, vocab) is never accepted and is reported
+    bad = tokens.copy()
+    bad[1] = case.vocab + 5
+    res = _run(case, q, bad, ua, ub, 1.0)
+    assert res["err"] == binding.SV_DEVERR_BAD_TREE
