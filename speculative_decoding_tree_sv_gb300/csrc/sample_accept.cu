@@ -338,6 +338,17 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kWalkThreads)
     s_z = z;
   }
   __syncthreads();
+  if (N < 1 || N > kMaxNodes) {
+    // no valid tree (reported above): nothing to draw from; every CTA of the
+    // cluster leaves here, before any cluster barrier
+    if (rank == 0 && threadIdx.x == 0) {
+      int* out_path = p.accepted_nodes + static_cast<size_t>(b) * (p.max_depth + 1);
+      for (int d = 0; d <= p.max_depth; ++d) out_path[d] = -1;
+      p.accept_len[b] = 0;
+      p.bonus[b] = -1;
+    }
+    return;
+  }
   const int z = s_z;
   const int t = n0 + z;
   const int nz = max(1, min(p.nz[t], kMaxZ));

@@ -164,3 +164,28 @@ def test_bad_inputs_are_reported_not_trapped():
     bad[1] = case.vocab + 5
     res = _run(case, q, bad, ua, ub, 1.0)
     assert res["err"] == binding.SV_DEVERR_BAD_TREE
+
+
+def test_empty_tree_in_a_batch_is_reported_with_defined_outputs():
+    case = make_case("tiny", batch=3)
+    q, tokens, ua, ub = make_sampling_inputs(case, seed=21)
+    # make the last sequence empty: its nodes are dropped from cu_nodes
+    n_last = int(case.cu_nodes[3] - case.cu_nodes[2])
+    T = int(case.cu_nodes[2])
+    trimmed = make_case("tiny", batch=3)
+    trimmed.cu_nodes = case.cu_nodes.copy()
+    trimmed.cu_nodes[3] = trimmed.cu_nodes[2]   # total_nodes follows cu_nodes
+    trimmed.logits = case.logits[:T]
+    trimmed.parents = case.parents[:T]
+    res = _run(trimmed, q[:T], tokens[:T], ua[:T], ub[:T], 1.0)
+    assert res["err"] == binding.SV_DEVERR_BAD_TREE
+    assert res["accept_len"][2] == 0 and res["bonus"][2] == -1
+    assert (res["accepted_nodes"][2] == -1).all()
+    two = make_case("tiny", batch=3)
+    two.cu_nodes, two.batch = case.cu_nodes[:3].copy(), 2
+    two.logits, two.parents = case.logits[:T], case.parents[:T]
+    ref = _oracle(two, q[:T], tokens[:T], ua[:T], ub[:T], 1.0)
+    for b in range(2):  # the other sequences are unaffected
+        if ref["walk_margin"][b] > TOL_ACCEPT:
+            assert list(res["accepted_nodes"][b][: res["accept_len"][b] + 1]) == ref["accepted_nodes"][b]
+    assert n_last >= 1
