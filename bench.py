@@ -36,6 +36,7 @@ if ROOT not in sys.path:
 
 METRIC = "tree-verify nodes/s per layer; attention HBM GB/s as % of GB300 peak (1 GPU)"
 UNIT = "nodes/s/layer"
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0  # TFLOP/s, one earlier GB300 measurement
 FALLBACK_HBM_GBS = 6800.0
 WORKLOADS = {
     "llama8b_eagle": "Llama-3.1-8B shaped verify step: batch 1, 32 layers x (32 q / 8 kv heads, head_dim 128), "
@@ -82,6 +83,17 @@ def measured_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tensor_peak():
+    """Sustained dense bf16 TFLOP/s (the attention is timed in a seconds-long
+    loop of launches), and whether it was measured here."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
 
 
 def measured_traffic(config: str):
@@ -444,6 +456,8 @@ def accept_commit_timing(torch, st, args, world, peak):
 def run_gpu(args):
     import torch
 
+    from synth import node_depths
+
     from speculative_decoding_tree_sv_gb300 import binding
     from speculative_decoding_tree_sv_gb300 import build as _build
     from speculative_decoding_tree_sv_gb300 import cost
@@ -494,6 +508,11 @@ def run_gpu(args):
     attn_launch_s = ms_attn * 1e-3 / (args.steps * c.num_layers)
     achieved = bytes_launch / attn_launch_s / 1e9
     peak, peak_kind = measured_peaks()
+    # past the ridge (large trees at large GQA) the tensor pipe is the bound
+    depths = [node_depths(c.parents[c.cu_nodes[b]:c.cu_nodes[b + 1]]) for b in range(c.batch)]
+    flops_launch = cost.attention_flops(ctx_keys, depths, c.num_q_heads, c.head_dim)
+    tpeak, tpeak_kind = measured_tensor_peak()
+    tensor_bound = flops_launch / bytes_launch > tpeak * 1e12 / (peak * 1e9)
     traffic = measured_traffic(args.config)
 
     # end to end through the public API with host buffers: pinned H2D of the
@@ -542,11 +561,19 @@ def run_gpu(args):
                        "l2": "inputs larger than L2 (distinct KV per layer, %.0f MB per step)"
                              % (sum(ctx_keys) * 4 * c.num_kv_heads * c.head_dim * c.num_layers / 1e6),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
-                         "kernel": "sv_tree_attention (attention + split combine)",
-                         "bytes_per_launch": bytes_launch, "launch_us": attn_launch_s * 1e6,
-                         "launch_us_without_graph": attn_eager_us},
+            "roofline": ({"bound": "tensor", "achieved": flops_launch / attn_launch_s / 1e12, "peak": tpeak,
+                          "unit": "TFLOP/s", "frac": flops_launch / attn_launch_s / 1e12 / tpeak,
+                          "traffic": traffic, "peak_kind": tpeak_kind + " (sustained bf16)",
+                          "kernel": "sv_tree_attention (attention + split combine)",
+                          "flops_per_launch": flops_launch, "bytes_per_launch": bytes_launch,
+                          "hbm_gbs": achieved, "hbm_frac": achieved / peak,
+                          "launch_us": attn_launch_s * 1e6, "launch_us_without_graph": attn_eager_us}
+                         if tensor_bound else
+                         {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                          "frac": achieved / peak, "traffic": traffic, "peak_kind": peak_kind,
+                          "kernel": "sv_tree_attention (attention + split combine)",
+                          "bytes_per_launch": bytes_launch, "flops_per_launch": flops_launch,
+                          "launch_us": attn_launch_s * 1e6, "launch_us_without_graph": attn_eager_us}),
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": st.launches_per_step() * args.steps,
