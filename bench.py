@@ -171,6 +171,12 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------- workload
 
+def _workload_seed(name: str) -> int:
+    from synth import CONFIGS
+    base = {"long_partial_pv": "long_partial"}.get(name, name)
+    return int(CONFIGS[base]["seed"])
+
+
 def build_case(name: str, seed_offset: int = 0):
     from synth import make_case
     if name == "llama8b_eagle":
@@ -557,7 +563,7 @@ def run_gpu(args):
                        "total_nodes": c.total_nodes, "kv_splits": st.splits,
                        "split_merge": "combine kernel" if st.split_reduce == 2 else "none",
                        "attention_kernel": ["paired 128-row CTAs", "256-row CTAs"][st.kernel],
-                       "cuda_graph": True, "early_context": bool(flags),
+                       "cuda_graph": True, "early_context": bool(flags), "seed": _workload_seed(args.config),
                        "l2": "inputs larger than L2 (distinct KV per layer, %.0f MB per step)"
                              % (sum(ctx_keys) * 4 * c.num_kv_heads * c.head_dim * c.num_layers / 1e6),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
