@@ -226,6 +226,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   // which is only useful once the partials are written (signalled at exit).
   if (p.reduce_mode == kReduceNone) griddep_launch_dependents();
   if (threadIdx.x == 0) mark(SV_TRACE_INPUTS);
+  // With the full context, tiles are dealt to the splits in turn (split s
+  // takes tiles s, s + S, ...), so a split's first tile is tile s whatever
+  // the context's length and the page-id warp requests its block-table
+  // entries before the length arrives.  A partial list keeps contiguous
+  // ranges (its ids come from the list itself, one read later anyway).
+  int spec_phys = 0;
+  bool spec_ok = false;
+  if (warp == 2 && lane < kPagesPerTile && p.kv_pages == nullptr) {
+    const int e = split * kPagesPerTile + lane;
+    if (e < p.max_pages_per_seq) {
+      spec_phys = p.block_table[static_cast<size_t>(b) * p.max_pages_per_seq + e];
+      spec_ok = true;
+    }
+  }
 
   const int n0 = p.cu_nodes[b];
   const int N = p.cu_nodes[b + 1] - n0;
@@ -253,9 +267,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int t_ctx = (n_pages + kPagesPerTile - 1) / kPagesPerTile;
   const int t_all = t_ctx + 1;  // + the tree tile
-  const int jb = static_cast<int>(static_cast<long long>(split) * t_all / p.num_splits);
-  const int je = static_cast<int>(static_cast<long long>(split + 1) * t_all / p.num_splits);
-  const int ntiles = je - jb;
+  const bool dealt = !partial;  // tiles dealt in turn (full context) or contiguous (partial list)
+  const int jb = dealt ? split : static_cast<int>(static_cast<long long>(split) * t_all / p.num_splits);
+  const int jstep = dealt ? p.num_splits : 1;
+  const int ntiles = dealt ? (split < t_all ? (t_all - 1 - split) / p.num_splits + 1 : 0)
+                           : static_cast<int>(static_cast<long long>(split + 1) * t_all / p.num_splits) - jb;
+  const bool owns_tree = ntiles > 0 && jb + (ntiles - 1) * jstep == t_all - 1;  // the last tile is the tree's
   const bool work = ntiles > 0;  // uniform over the pair
 
   if (!work && p.reduce_mode == kReduceGlobal) {
@@ -277,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ahead of the loaders.
       bool ok = true;
       for (int it = 0; it < ntiles; ++it) {
-        const int j = jb + it;
+        const int j = jb + it * jstep;
         const int sl = it % kIdSlots;
         if (it >= kIdSlots) {
           int w = (lane == 0) ? (mbar_wait(ids_empty + sl, ((it / kIdSlots) & 1) ^ 1u, abort_flag) ? 1 : 0) : 0;
@@ -290,7 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             report_error(p.err, SV_DEVERR_BAD_PAGE);
             lp = 0;
           }
-          int phys = p.block_table[static_cast<size_t>(b) * p.max_pages_per_seq + lp];
+          int phys = (it == 0 && spec_ok && lp == split * kPagesPerTile + lane)
+                         ? spec_phys
+                         : p.block_table[static_cast<size_t>(b) * p.max_pages_per_seq + lp];
           if (phys < 0 || phys >= p.num_pages) {
             report_error(p.err, SV_DEVERR_BAD_PAGE);
             phys = 0;
@@ -326,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       // one tile into the ring; false when a bounded wait ran out
       auto load_tile = [&](int it) -> bool {
-        const int j = jb + it;
+        const int j = jb + it * jstep;
         const int st = it % NS;
         const uint32_t ph = (it / NS) & 1;
         const int sl = it % kIdSlots;
@@ -371,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.early_ctx) {
         // Context pages are not written by the preceding grid: the first
         // ring's worth of them is requested before waiting for it.
-        for (; ok && it < ntiles && it < NS && jb + it < t_ctx; ++it) ok = load_tile(it);
+        for (; ok && it < ntiles && it < NS && jb + it * jstep < t_ctx; ++it) ok = load_tile(it);
       }
       griddep_wait();  // the tree's K/V come from the preceding grid
       for (; ok && it < ntiles; ++it) ok = load_tile(it);
@@ -500,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // owns the tree tile needs it): the tree's parents are staged in shared
       // memory with one coalesced load, then each row walks its chain there
       uint32_t anc0 = 0, anc1 = 0, anc2 = 0, anc3 = 0;
-      if (je == t_all) {
+      if (owns_tree) {
         for (int i = r; i < N && i < kMaxNodes; i += kTileRows) par_s[i] = p.parents[n0 + i];
         named_barrier(1, kTileRows);
         if (row_exists) {
@@ -523,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (r == 0) mark(SV_TRACE_TREE_MASK);
       }
       for (int it = 0; it < ntiles; ++it) {
-        const int j = jb + it;
+        const int j = jb + it * jstep;
         const int buf = it & 1;
         const uint32_t col_s = buf ? C::kColS1 : C::kColS0;
         // warp-uniform outcome: the TMEM loads below are warp-collective
