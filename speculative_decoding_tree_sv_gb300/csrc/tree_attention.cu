@@ -657,18 +657,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* stage = smem + C::kOffStage + qw * 32 * C::kStageStride;
       uint8_t* mine = stage + lane * C::kStageStride;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(lane_base + C::kColO + c * 32, o);
+      for (int c = 0; c < D / 32; c += 2) {
+        uint32_t o[2][32];
+        tmem_ld32(lane_base + C::kColO + c * 32, o[0]);
+        tmem_ld32(lane_base + C::kColO + (c + 1) * 32, o[1]);
         tmem_ld_wait();
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
           uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
-          w.y = pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
-          w.z = pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
-          w.w = pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
-          reinterpret_cast<uint4*>(mine + c * 64)[v] = w;
+          w.x = pack_bf16x2(__uint_as_float(o[h][8 * v + 0]) * inv_l, __uint_as_float(o[h][8 * v + 1]) * inv_l);
+          w.y = pack_bf16x2(__uint_as_float(o[h][8 * v + 2]) * inv_l, __uint_as_float(o[h][8 * v + 3]) * inv_l);
+          w.z = pack_bf16x2(__uint_as_float(o[h][8 * v + 4]) * inv_l, __uint_as_float(o[h][8 * v + 5]) * inv_l);
+          w.w = pack_bf16x2(__uint_as_float(o[h][8 * v + 6]) * inv_l, __uint_as_float(o[h][8 * v + 7]) * inv_l);
+          reinterpret_cast<uint4*>(mine + (c + h) * 64)[v] = w;
         }
       }
       __syncwarp();
@@ -681,12 +684,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t split_base = partial_out ? static_cast<size_t>(split) * p.total_nodes * p.num_q_heads : 0;
       const long long my_out_row = static_cast<long long>(split_base + orow);  // this lane's row
       __nv_bfloat16* const base = partial_out ? p.part_o : p.out;
-      for (int rb = 0; rb < nrows; rb += kRowsPerPass) {
-        const int rr = rb + lane / kChunks;
-        const long long grow_out = __shfl_sync(0xffffffffu, my_out_row, min(rr, 31));
-        if (rr < nrows)
-          reinterpret_cast<uint4*>(base + grow_out * D)[lane % kChunks] =
-              reinterpret_cast<const uint4*>(stage + rr * C::kStageStride)[lane % kChunks];
+      // every shuffle and staging load is issued before the first store
+      constexpr int kPasses = 32 / kRowsPerPass;
+      uint4 val[kPasses];
+      long long gout[kPasses];
+#pragma unroll
+      for (int i = 0; i < kPasses; ++i) {
+        const int rr = i * kRowsPerPass + lane / kChunks;
+        gout[i] = __shfl_sync(0xffffffffu, my_out_row, rr);
+        val[i] = reinterpret_cast<const uint4*>(stage + rr * C::kStageStride)[lane % kChunks];
+      }
+#pragma unroll
+      for (int i = 0; i < kPasses; ++i) {
+        const int rr = i * kRowsPerPass + lane / kChunks;
+        if (rr < nrows) reinterpret_cast<uint4*>(base + gout[i] * D)[lane % kChunks] = val[i];
       }
     }
     if (p.reduce_mode == kReduceNone) {

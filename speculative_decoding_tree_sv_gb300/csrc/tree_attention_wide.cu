@@ -544,12 +544,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const size_t split_base = partial_out ? static_cast<size_t>(split) * p.total_nodes * p.num_q_heads : 0;
       const long long my_out_row = static_cast<long long>(split_base + orow);  // this lane's row
       __nv_bfloat16* const base = partial_out ? p.part_o : p.out;
-      for (int rb = 0; rb < nrows; rb += kRowsPerPass) {
-        const int rr = rb + lane / kChunks;
-        const long long grow_out = __shfl_sync(0xffffffffu, my_out_row, min(rr, 31));
-        if (rr < nrows)
-          reinterpret_cast<uint4*>(base + grow_out * D)[lane % kChunks] =
-              reinterpret_cast<const uint4*>(stage + rr * C::kStageStride)[lane % kChunks];
+      // every shuffle and staging load is issued before the first store
+      constexpr int kPasses = 32 / kRowsPerPass;
+      uint4 val[kPasses];
+      long long gout[kPasses];
+#pragma unroll
+      for (int i = 0; i < kPasses; ++i) {
+        const int rr = i * kRowsPerPass + lane / kChunks;
+        gout[i] = __shfl_sync(0xffffffffu, my_out_row, rr);
+        val[i] = reinterpret_cast<const uint4*>(stage + rr * C::kStageStride)[lane % kChunks];
+      }
+#pragma unroll
+      for (int i = 0; i < kPasses; ++i) {
+        const int rr = i * kRowsPerPass + lane / kChunks;
+        if (rr < nrows) reinterpret_cast<uint4*>(base + gout[i] * D)[lane % kChunks] = val[i];
       }
     }
     if (p.reduce_mode == kReduceNone) {
