@@ -211,9 +211,17 @@ class GpuStep:
 
         self.T, self.Hq, self.Hkv, self.D = c.total_nodes, c.num_q_heads, c.num_kv_heads, c.head_dim
         self.layers = c.num_layers
-        self.q = bf(c.q)
-        self.tree_k = bf(c.tree_k)
-        self.tree_v = bf(c.tree_v)
+        # each layer's Q, tree K and tree V sit side by side in one arena row,
+        # so one host-to-device copy moves a layer's (or a run of layers')
+        # per-step inputs
+        nq, nk = int(np.prod(c.q.shape[1:])), int(np.prod(c.tree_k.shape[1:]))
+        self.layer_arena = torch.empty((c.num_layers, nq + 2 * nk), dtype=torch.bfloat16, device=dev)
+        self.q = self.layer_arena[:, :nq].view(c.q.shape)
+        self.tree_k = self.layer_arena[:, nq:nq + nk].view(c.tree_k.shape)
+        self.tree_v = self.layer_arena[:, nq + nk:].view(c.tree_v.shape)
+        self.q.copy_(bf(c.q))
+        self.tree_k.copy_(bf(c.tree_k))
+        self.tree_v.copy_(bf(c.tree_v))
         self.k_cache = bf(c.k_cache)
         self.v_cache = bf(c.v_cache)
         self.block_table = i32(c.block_table)
@@ -262,7 +270,7 @@ class GpuStep:
         c, b = self.case, self.binding
         b.sv_greedy_accept(self.logits, c.vocab, self.tokens, self.parents, self.cu_nodes, c.batch, self.T,
                            c.max_nodes, c.max_depth, self.am, self.alen, self.anodes, self.bonus, self.ws_acc)
-        b.sv_kv_commit(self.tree_k, self.tree_v, self.T * self.Hkv * self.D, self.k_cache, self.v_cache,
+        b.sv_kv_commit(self.tree_k, self.tree_v, self.tree_k.stride(0), self.k_cache, self.v_cache,
                        c.num_pages * self.Hkv * c.page_size * self.D, self.layers, c.num_pages,
                        self.block_table, c.max_pages_per_seq, self.ctx_lens, self.cu_nodes, self.anodes,
                        self.alen, c.batch, c.max_depth, self.Hkv, self.D, c.page_size, self.new_lens, self.ws)
@@ -422,7 +430,7 @@ def accept_commit_timing(torch, st, args, world, peak):
                                c.max_depth, st.am, st.alen, st.anodes, st.bonus, st.ws_acc)
 
     def commit_only():
-        b.sv_kv_commit(st.tree_k, st.tree_v, st.T * st.Hkv * st.D, st.k_cache, st.v_cache,
+        b.sv_kv_commit(st.tree_k, st.tree_v, st.tree_k.stride(0), st.k_cache, st.v_cache,
                        c.num_pages * st.Hkv * c.page_size * st.D, st.layers, c.num_pages, st.block_table,
                        c.max_pages_per_seq, st.ctx_lens, st.cu_nodes, st.anodes, st.alen, c.batch, c.max_depth,
                        st.Hkv, st.D, c.page_size, st.new_lens, st.ws)
@@ -525,7 +533,7 @@ def run_gpu(args):
     # step's inputs, the step, D2H of the results; captured like the step.
     pin = {}
     h2d = 0
-    for name in ("q", "tree_k", "tree_v", "logits", "parents", "tokens", "cu_nodes", "ctx_lens"):
+    for name in ("layer_arena", "logits", "parents", "tokens", "cu_nodes", "ctx_lens"):
         t = getattr(st, name)
         pin[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
         h2d += t.numel() * t.element_size()
@@ -533,14 +541,49 @@ def run_gpu(args):
                 for n in ("alen", "anodes", "bonus")}
     d2h = sum(v.numel() * 4 for v in res_host.values())
 
+    # The copies run on a second stream in the order the step consumes them:
+    # the index arrays, then the layers' Q / tree K / tree V in runs of 1, 4,
+    # 16, ... layers (a layer's inputs copy about four times faster than its
+    # attention runs, so each run lands while the runs before it are being
+    # computed), then the logits and tokens.  The first call of each run
+    # waits for that run; a cross-stream wait costs a few microseconds in the
+    # replayed graph, so there is one per run, not one per layer.
+    copy_stream = torch.cuda.Stream()
+    first = ("parents", "cu_nodes", "ctx_lens")
+    last = ("logits", "tokens")
+    assert set(first + last + ("layer_arena",)) == set(pin)
+    runs, l0, n = [], 0, 1
+    while l0 < st.layers:
+        runs.append((l0, min(st.layers, l0 + n)))
+        l0, n = runs[-1][1], 4 * n
+
     def e2e_step():
-        for name, h in pin.items():
-            getattr(st, name).copy_(h, non_blocking=True)
-        st.step()
+        cur = torch.cuda.current_stream()
+        copy_stream.wait_stream(cur)
+        run_ready = {}
+        with torch.cuda.stream(copy_stream):
+            for name in first:
+                getattr(st, name).copy_(pin[name], non_blocking=True)
+            for a, b in runs:
+                st.layer_arena[a:b].copy_(pin["layer_arena"][a:b], non_blocking=True)
+                run_ready[a] = torch.cuda.Event()
+                run_ready[a].record(copy_stream)
+            for name in last:
+                getattr(st, name).copy_(pin[name], non_blocking=True)
+        for li, p in enumerate(st.params):
+            if li in run_ready:
+                cur.wait_event(run_ready[li])
+            st.binding.sv_tree_attention(p)
+        cur.wait_stream(copy_stream)
+        st.accept_and_commit()
         for n, h in res_host.items():
             h.copy_(getattr(st, n), non_blocking=True)
 
     ms_e2e, _ge = _time_graph(torch, e2e_step, args.steps, args.warmup, world)
+    # the synthetic logits plant each sequence's accepted path: the lengths
+    # read back through the timed path must be those
+    if not np.array_equal(res_host["alen"].numpy(), np.asarray(c.planted_len)):
+        raise RuntimeError("accepted lengths read back differ from the planted paths")
     e2e_value = world * nodes_per_step / (ms_e2e * 1e-3 / args.steps)
 
     retrieval = retrieval_timing(torch, st, args, world) if partial else None
