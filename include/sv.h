@@ -264,7 +264,8 @@ sv_status sv_greedy_accept_noalloc(const float* logits, int vocab, const int* to
  *   accepted_child (optional) int32 [total_nodes]: per node the local index
  *                of its accepted child, -1 if none
  *   accept_len, accepted_nodes, bonus_token: as for sv_greedy_accept.
- * vocab >= 8 and <= 2^24; temperature > 0 and finite; max_nodes <= 128.
+ * vocab >= 8 and <= 2^18 (262144); temperature > 0 and finite;
+ * max_nodes <= 128.  A larger vocabulary returns SV_ERR_UNSUPPORTED.
  * The workspace (sv_sample_accept_workspace_size bytes) holds per-node
  * scalars between the two launches; it needs no zeroing between calls.
  * ---------------------------------------------------------------------- */

@@ -131,6 +131,7 @@ def test_sample_accept_host_validation(lib):
     assert call(temp=float("nan")) == 1
     assert call(vocab=4) == 1                         # below one entry per CTA of a cluster
     assert call(max_nodes=129) == 2
+    assert call(vocab=(1 << 18) + 1) == 2                 # eight 2^15-entry slices at most
     assert call(vocab=(1 << 24) + 1) == 2
     assert call(ws_bytes=need - 1) == 4
     assert call(total=0) == 0                         # nothing to do, nothing launched
