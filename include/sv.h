@@ -120,7 +120,7 @@ enum sv_attn_flags {
 
 typedef struct sv_attn_params {
   /* shapes (host values) */
-  int batch;              /* B >= 1                                          */
+  int batch;              /* B, 1..65535                                     */
   int num_q_heads;        /* Hq                                              */
   int num_kv_heads;       /* Hkv; G = Hq / Hkv must be 1, 2, 4, 8 or 16     */
   int head_dim;           /* D: 64 or 128                                    */
@@ -172,7 +172,8 @@ sv_status sv_tree_attention_plan(const sv_attn_params* params, int* num_splits, 
 /* Launches the attention (and, with more than one split, the split combine)
  * on `stream`: one CTA per (KV split, KV head x 128-row tile, sequence) for
  * the paired kernel or per (KV split, KV head x 256-row group, sequence) for
- * the wide one (sv_attn_flags). */
+ * the wide one (sv_attn_flags).  Hkv x (ceil(max_nodes x G / 128) + 1) must
+ * not exceed 65535 (SV_ERR_UNSUPPORTED otherwise). */
 sv_status sv_tree_attention(const sv_attn_params* params, sv_stream_t stream);
 
 /* ------------------------------------------------------------------------
@@ -198,6 +199,8 @@ sv_status sv_tree_attention(const sv_attn_params* params, sv_stream_t stream);
  * logits: fp32 [T, vocab], rows contiguous.  tokens/parents: int32 [T]
  * (tokens[root] unused).  max_nodes (host) <= 128.  max_depth (host) is the
  * row stride - 1 of accepted_nodes and must be >= every tree's depth.
+ * total_nodes <= 65535 (one grid row per node); a larger call returns
+ * SV_ERR_UNSUPPORTED.
  * ---------------------------------------------------------------------- */
 sv_status sv_greedy_accept_workspace_size(int batch, int total_nodes, size_t* bytes);
 
@@ -298,7 +301,8 @@ sv_status sv_sample_accept(const float* logits, const float* draft_probs, int vo
  * [num_layers][num_pages, Hkv, page_size, D], layer stride
  * cache_layer_stride elements.  Both strides are multiples of 8.
  * workspace is optional (NULL, or >= 256 bytes zero-filled once) and only
- * receives the error word.
+ * receives the error word.  head_dim is a multiple of 8; max_depth + 1,
+ * batch and num_layers are each <= 65535 (SV_ERR_UNSUPPORTED otherwise).
  * ---------------------------------------------------------------------- */
 sv_status sv_kv_commit(const void* tree_k, const void* tree_v, long long tree_layer_stride,
                        void* k_cache, void* v_cache, long long cache_layer_stride,
