@@ -118,9 +118,9 @@ def measured_traffic(config: str):
 class ClockSampler:
     """Samples SM clocks and throttle reasons with nvidia-smi while running."""
 
-    def __init__(self, device_index: int):
+    def __init__(self, device_index: int, out_dir: str):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+        self.path = os.path.join(out_dir, f"clocks_rank{device_index}.csv")
         self.dev = device_index
 
     def __enter__(self):
@@ -490,7 +490,7 @@ def run_gpu(args):
     nodes_per_step = c.total_nodes * c.num_layers
 
     # whole step, graph-replayed, clocks sampled meanwhile
-    with ClockSampler(local) as clk:
+    with ClockSampler(local, args.clocks_dir) as clk:
         ms, _g = _time_graph(torch, st.step, args.steps, args.warmup, world)
         # attention alone (the dominant kernel) for the roofline
         ms_attn, _ga = _time_graph(torch, st.attention_all_layers, args.steps, args.warmup, world)
@@ -645,6 +645,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["sv", "reference"], default="sv")
     ap.add_argument("--config", choices=sorted(WORKLOADS), default="llama8b_eagle")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-dir", default=os.path.join(ROOT, "bench_out"),
+                    help="where the nvidia-smi clock samples of the timed region are written")
     ap.add_argument("--early-context", action="store_true",
                     help="launch attention with SV_ATTN_EARLY_CONTEXT")
     args = ap.parse_args(argv)
