@@ -309,6 +309,34 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   return d;
 }
 
+// Sequence order of a batched launch.  The block scheduler dispatches CTAs
+// in grid order, and a batch whose (sequence, head) units outnumber the
+// resident CTAs runs in waves; dispatching the longest sequences first lets
+// the shorter ones fill the SMs that the first wave frees, which shortens the
+// last wave (longest-processing-time-first list scheduling).  Returns the
+// sequence whose key (context length, or listed pages with a partial list)
+// is the r-th largest, ties to the lower index, for batches of 2..64
+// sequences, and r itself otherwise.  Warp-wide: every lane calls it with
+// the same arguments.
+__device__ __forceinline__ int longest_first_seq(int r, int batch, const int* ctx_lens, const int* cu_kv_pages) {
+  if (batch <= 1 || batch > 64) return r;
+  const int lane = threadIdx.x & 31;
+  auto key = [&](int s) -> int {
+    if (s >= batch) return 0;
+    return cu_kv_pages != nullptr ? cu_kv_pages[s + 1] - cu_kv_pages[s] : ctx_lens[s];
+  };
+  const int k0 = key(lane), k1 = key(lane + 32);
+  int rank0 = 0, rank1 = 0;
+  for (int j = 0; j < batch; ++j) {
+    const int kj = __shfl_sync(0xffffffffu, j < 32 ? k0 : k1, j & 31);
+    rank0 += (kj > k0 || (kj == k0 && j < lane)) ? 1 : 0;
+    rank1 += (kj > k1 || (kj == k1 && j < lane + 32)) ? 1 : 0;
+  }
+  const unsigned m0 = __ballot_sync(0xffffffffu, lane < batch && rank0 == r);
+  const unsigned m1 = __ballot_sync(0xffffffffu, lane + 32 < batch && rank1 == r);
+  return m0 ? __ffs(m0) - 1 : (m1 ? 31 + __ffs(m1) : r);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

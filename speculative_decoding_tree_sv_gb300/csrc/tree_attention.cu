@@ -132,7 +132,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int split = blockIdx.x;
   const int kh = blockIdx.y / p.row_tiles;
   const int rt = blockIdx.y % p.row_tiles;
-  const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.group;
@@ -226,6 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // which is only useful once the partials are written (signalled at exit).
   if (p.reduce_mode == kReduceNone) griddep_launch_dependents();
   if (threadIdx.x == 0) mark(SV_TRACE_INPUTS);
+  // the z-th longest sequence (batches of up to 64; the index itself beyond)
+  const int b = longest_first_seq(blockIdx.z, gridDim.z, p.ctx_lens, p.cu_kv_pages);
   // With the full context, tiles are dealt to the splits in turn (split s
   // takes tiles s, s + S, ...), so a split's first tile is tile s whatever
   // the context's length and the page-id warp requests its block-table

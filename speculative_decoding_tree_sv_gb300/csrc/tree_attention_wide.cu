@@ -105,7 +105,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int split = blockIdx.x;
   const int kh = blockIdx.y / p.groups_per_seq;
   const int mg = blockIdx.y % p.groups_per_seq;
-  const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.group;
@@ -179,6 +178,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (p.reduce_mode == kReduceNone) griddep_launch_dependents();
   if (threadIdx.x == 0) mark(SV_TRACE_INPUTS);
 
+  // the z-th longest sequence (batches of up to 64; the index itself beyond)
+  const int b = longest_first_seq(blockIdx.z, gridDim.z, p.ctx_lens, p.cu_kv_pages);
   const int n0 = p.cu_nodes[b];
   const int N = p.cu_nodes[b + 1] - n0;
   const int L = p.ctx_lens[b];

@@ -3,7 +3,8 @@ oracle: |out - oracle| <= 2e-2 elementwise (bf16 inputs, fp32 accumulation),
 log-sum-exp within 2e-3.  Covers the five workloads (sampled where the
 oracle would take too long), several split counts, GQA groups 1..16, both
 head sizes, ragged and empty contexts, root-only and 128-node chain trees,
-partial page lists (empty, complete, SpecPV's small settings) and the
+partial page lists (empty, complete, SpecPV's small settings), batches on
+both sides of the 64-sequence limit of longest-first dispatch, and the
 device error word."""
 
 import numpy as np
@@ -150,6 +151,18 @@ def test_ragged_and_empty_contexts(ctx, kernel):
     case = make_case("tiny", batch=len(ctx), ctx=ctx, seed=sum(ctx) + 7, with_logits=False)
     _check(case, num_splits=0, flags=kernel)
     _check(case, num_splits=3, flags=kernel)
+    _check(case, num_splits=3, split_reduce=2, flags=kernel)
+
+
+@pytest.mark.parametrize("batch", [64, 70])
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_batch_order_limit_with_tied_lengths(batch, kernel):
+    # up to 64 sequences are dispatched longest first (ties by index); more
+    # are dispatched in index order; lengths repeat so the order has ties
+    rng = np.random.default_rng(batch)
+    ctx = [int(x) for x in rng.choice([0, 17, 128, 129, 300], size=batch)]
+    case = make_case("tiny", batch=batch, ctx=ctx, seed=batch, with_logits=False)
+    _check(case, flags=kernel)
     _check(case, num_splits=3, split_reduce=2, flags=kernel)
 
 
