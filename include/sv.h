@@ -172,8 +172,10 @@ sv_status sv_tree_attention_plan(const sv_attn_params* params, int* num_splits, 
 /* Launches the attention (and, with more than one split, the split combine)
  * on `stream`: one CTA per (KV split, KV head x 128-row tile, sequence) for
  * the paired kernel or per (KV split, KV head x 256-row group, sequence) for
- * the wide one (sv_attn_flags).  Hkv x (ceil(max_nodes x G / 128) + 1) must
- * not exceed 65535 (SV_ERR_UNSUPPORTED otherwise). */
+ * the wide one (sv_attn_flags); in batches of 2..64 sequences the longest
+ * (context length, or listed pages) are dispatched first.  Hkv x
+ * (ceil(max_nodes x G / 128) + 1) must not exceed 65535 (SV_ERR_UNSUPPORTED
+ * otherwise). */
 sv_status sv_tree_attention(const sv_attn_params* params, sv_stream_t stream);
 
 /* ------------------------------------------------------------------------
