@@ -311,6 +311,9 @@ def _time_graph(torch, fn, steps: int, warmup: int, world: int):
 
 # ---------------------------------------------------------------------------- CPU oracle leg
 
+CPU_BASELINE_SECONDS = 10.0
+
+
 def oracle_step_seconds(case, partial: bool, attn_layers: int = 1):
     """Times the oracle on `attn_layers` layers of attention plus one
     acceptance and one full commit; returns (seconds per full step, detail)."""
@@ -591,11 +594,19 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        s, detail = oracle_step_seconds(case, partial)
+        # whole steps (every layer's attention, the acceptance, the commit),
+        # repeated until about ten seconds of host work have been timed
+        t_start, n_steps, details = time.perf_counter(), 0, []
+        while n_steps == 0 or time.perf_counter() - t_start < CPU_BASELINE_SECONDS:
+            details.append(oracle_step_seconds(case, partial, attn_layers=c.num_layers)[1])
+            n_steps += 1
+        s = (time.perf_counter() - t_start) / n_steps
+        mean = {k: statistics.mean(d[k] for d in details) for k in details[0]}
         cpu = {"value": nodes_per_step / s, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-               "sample": f"oracle (NumPy fp64) attention on 1 of {c.num_layers} layers scaled x{c.num_layers}, "
-                         f"acceptance over all {c.total_nodes}x{c.vocab} logits and the commit of all layers: "
-                         + ", ".join(f"{k} {v:.3f}" for k, v in detail.items())}
+               "sample": f"oracle (NumPy fp64): {n_steps} whole steps of the workload ({c.num_layers} layers of "
+                         f"attention, acceptance over all {c.total_nodes}x{c.vocab} logits, the commit of all "
+                         f"layers) in {s * n_steps:.1f} s; per step "
+                         + ", ".join(f"{k} {v:.3f}" for k, v in mean.items())}
 
     if rank == 0:
         line = {
