@@ -314,6 +314,17 @@ def _time_graph(torch, fn, steps: int, warmup: int, world: int):
 CPU_BASELINE_SECONDS = 10.0
 
 
+def copy_runs(layers: int, growth: int = 4):
+    """Half-open layer ranges [a, b) of 1, growth, growth^2, ... layers that
+    cover 0 .. layers - 1 in order: the host-to-device copies of the
+    end-to-end step, one per range."""
+    runs, a, n = [], 0, 1
+    while a < layers:
+        runs.append((a, min(layers, a + n)))
+        a, n = runs[-1][1], growth * n
+    return runs
+
+
 def oracle_step_seconds(case, partial: bool, attn_layers: int = 1):
     """Times the oracle on `attn_layers` layers of attention plus one
     acceptance and one full commit; returns (seconds per full step, detail)."""
@@ -555,10 +566,7 @@ def run_gpu(args):
     first = ("parents", "cu_nodes", "ctx_lens")
     last = ("logits", "tokens")
     assert set(first + last + ("layer_arena",)) == set(pin)
-    runs, l0, n = [], 0, 1
-    while l0 < st.layers:
-        runs.append((l0, min(st.layers, l0 + n)))
-        l0, n = runs[-1][1], 4 * n
+    runs = copy_runs(st.layers)
 
     def e2e_step():
         cur = torch.cuda.current_stream()
@@ -579,8 +587,8 @@ def run_gpu(args):
             st.binding.sv_tree_attention(p)
         cur.wait_stream(copy_stream)
         st.accept_and_commit()
-        for n, h in res_host.items():
-            h.copy_(getattr(st, n), non_blocking=True)
+        for name, h in res_host.items():
+            h.copy_(getattr(st, name), non_blocking=True)
 
     ms_e2e, _ge = _time_graph(torch, e2e_step, args.steps, args.warmup, world)
     # the synthetic logits plant each sequence's accepted path: the lengths
