@@ -1,6 +1,7 @@
 """Bit-exact parity of sv_greedy_accept and sv_kv_commit (CUDA, through the
 C ABI) with the oracle: every workload's planted path, thousands of tiny
-random trees with duplicate sibling tokens and tied logits, ties across
+random trees with duplicate sibling tokens and tied logits, large trees
+(60..128 nodes, depth up to 127) whose accepted paths tie for depth, ties across
 vocabulary chunks, signed zeros, repeated calls on one workspace, and the
 commit of every layer checked byte for byte with sentinel-filled caches."""
 
@@ -89,6 +90,63 @@ def test_tiny_random_trees_with_ties_and_duplicates(V):
     for _ in range(40):
         c = _tiny_batch(rng, 64, V)
         ref = oracle.greedy_accept(c.logits, c.tokens, c.parents, c.cu_nodes)
+        _assert_accept_equal(run_accept(c), ref, c)
+
+
+def _big_batch(rng, B, V, shape):
+    # trees of 60..128 nodes over a tiny vocabulary, so many accepted paths
+    # tie for the greatest depth; "deep" trees hang each node up to three
+    # places below the previous one (depth ~60) and match their parent's
+    # arg-max nine times in ten, "chain" is a 128-node path whose every node
+    # matches
+    parents, tokens, rows, cu = [], [], [], [0]
+    for _ in range(B):
+        if shape == "chain":
+            n = 128
+            par = [-1] + list(range(n - 1))
+        else:
+            n = int(rng.integers(60, 129))
+            if shape == "deep":
+                par = [-1] + [max(0, i - 1 - int(rng.integers(0, 3))) for i in range(1, n)]
+            else:
+                par = [-1] + [int(rng.integers(0, i)) for i in range(1, n)]
+        lg = rng.standard_normal((n, V)).astype(np.float32)
+        tok = rng.integers(0, V, size=n)
+        if shape in ("chain", "deep"):
+            best = np.argmax(lg[np.array(par[1:])], axis=1)
+            keep = rng.random(n - 1) < (1.0 if shape == "chain" else 0.9)
+            tok[1:] = np.where(keep, best, tok[1:])
+        parents += par
+        tokens += tok.tolist()
+        rows.append(lg)
+        cu.append(cu[-1] + n)
+    c = _Tiny()
+    c.logits = np.concatenate(rows)
+    c.tokens = np.array(tokens, np.int32)
+    c.parents = np.array(parents, np.int32)
+    c.cu_nodes = np.array(cu, np.int32)
+    c.batch, c.vocab = B, V
+    c.total_nodes = cu[-1]
+    c.max_nodes = int(np.diff(cu).max())
+    depth = []
+    for b in range(B):
+        par = c.parents[cu[b]:cu[b + 1]]
+        d = np.zeros(len(par), np.int64)
+        for i in range(1, len(par)):
+            d[i] = d[par[i]] + 1
+        depth.append(int(d.max()))
+    c.max_depth = max(depth)
+    return c
+
+
+@pytest.mark.parametrize("shape,V", [("random", 2), ("random", 3), ("deep", 2), ("deep", 3), ("chain", 5)])
+def test_large_trees_with_many_tied_accepted_paths(shape, V):
+    rng = np.random.default_rng(1000 + V + len(shape))
+    for _ in range(4):
+        c = _big_batch(rng, 16, V, shape)
+        ref = oracle.greedy_accept(c.logits, c.tokens, c.parents, c.cu_nodes)
+        if shape == "chain":
+            assert (ref["accept_len"] == 127).all()
         _assert_accept_equal(run_accept(c), ref, c)
 
 
