@@ -190,6 +190,15 @@ def test_retrieval_host_validation(lib):
     assert f(a, 10, 8, 128, 16, a, 4, a, None, 1, 4, a, a, 8, None) == 4
 
 
+def test_partial_list_extend_host_validation(lib):
+    a = 1 << 20
+    f = lib.sv_partial_list_extend
+    assert f(None, a, a, a, 2, a, a, None, 0, None) == 1      # no refresh list
+    assert f(a, a, a, a, 0, a, a, None, 0, None) == 1         # empty batch
+    assert f(a, a, a, a, 2, None, a, None, 0, None) == 1      # no output list
+    assert f(a, a, a, a, 2, a, a, a, 16, None) == 4           # workspace below its header
+
+
 def test_specpv_schedule_matches_the_oracle(lib):
     import oracle
     rng = np.random.default_rng(0)
