@@ -20,3 +20,23 @@ def test_copy_runs_cover_the_layers_in_order(layers):
 
 def test_copy_runs_of_the_llama_step():
     assert bench.copy_runs(32) == [(0, 1), (1, 5), (5, 21), (21, 32)]
+
+
+def test_reference_arm_prints_one_contract_line():
+    # the reference arm times the CPU oracle; it needs no GPU
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=root, check=True).stdout
+    lines = [l for l in out.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"] == bench.WORKLOADS["llama8b_eagle"]
