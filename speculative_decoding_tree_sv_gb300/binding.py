@@ -137,10 +137,15 @@ def load(path: Optional[str] = None):
 
 
 def _ptr(x) -> Optional[int]:
+    """Address of a device buffer: None, a raw device address, or a CUDA
+    tensor.  A tensor in host memory is refused here, before the library
+    could hand its address to a kernel."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
+    if getattr(x, "is_cuda", True) is False:
+        raise ValueError(f"the library takes device memory; got a tensor on {x.device}")
     return int(x.data_ptr())
 
 

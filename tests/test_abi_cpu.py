@@ -190,6 +190,20 @@ def test_retrieval_host_validation(lib):
     assert f(a, 10, 8, 128, 16, a, 4, a, None, 1, 4, a, a, 8, None) == 4
 
 
+def test_host_tensors_are_refused_before_any_call(lib):
+    import torch
+    logits = torch.zeros(4, 8)                        # host memory
+    with pytest.raises(ValueError):
+        binding.sv_greedy_accept(logits, 8, 1 << 20, 1 << 20, 1 << 20, 1, 4, 4, 3, None, 1 << 20, 1 << 20,
+                                 1 << 20, 1 << 20, workspace_bytes=4096)
+    with pytest.raises(ValueError):
+        binding.make_attn_params(q=torch.zeros(4, 8, 64, dtype=torch.bfloat16), tree_k=1 << 20, tree_v=1 << 20,
+                                 k_cache=1 << 20, v_cache=1 << 20, block_table=1 << 20, ctx_lens=1 << 20,
+                                 cu_nodes=1 << 20, parents=1 << 20, out=1 << 20, total_nodes=4, max_nodes=4,
+                                 batch=1, num_q_heads=8, num_kv_heads=2, head_dim=64, num_pages=10,
+                                 max_pages_per_seq=10)
+
+
 def test_partial_list_extend_host_validation(lib):
     a = 1 << 20
     f = lib.sv_partial_list_extend
