@@ -202,7 +202,10 @@ sv_status sv_tree_attention(const sv_attn_params* params, sv_stream_t stream);
  * (tokens[root] unused).  max_nodes (host) <= 128.  max_depth (host) is the
  * row stride - 1 of accepted_nodes and must be >= every tree's depth.
  * total_nodes <= 65535 (one grid row per node); a larger call returns
- * SV_ERR_UNSUPPORTED.
+ * SV_ERR_UNSUPPORTED.  A sequence whose tree (from the device cu_nodes) has
+ * no node or more than 128 is not walked: it gets accept_len 0, bonus_token
+ * -1 and a path of -1, and the error word records SV_DEVERR_BAD_TREE; the
+ * workspace stays ready for the next call.
  * ---------------------------------------------------------------------- */
 sv_status sv_greedy_accept_workspace_size(int batch, int total_nodes, size_t* bytes);
 
@@ -226,8 +229,13 @@ sv_status sv_greedy_accept(const float* logits, int vocab, const int* tokens,
  *   - Limits: batch <= 1024 and total_nodes <= 8192; larger calls return
  *     SV_ERR_UNSUPPORTED without launching anything.
  *   - The first call on each device looks up that array's device address (a
- *     host-side driver query, with the device current); make that first call
- *     before any stream capture.
+ *     host-side driver query, with the device current).  With CUDA's lazy
+ *     module loading (the default) that first lookup also loads this
+ *     library's device code onto the device, which takes device memory once;
+ *     so make the first call during warm-up, before any stream capture and
+ *     before the point after which the caller may not allocate.  The address
+ *     is looked up again when the device's context changes (after a
+ *     cudaDeviceReset), and that call loads the device code again.
  *   - Every call uses the same array and clears the part it needs at its
  *     start, so calls that may overlap on the GPU (different streams, or
  *     different host threads without ordering) race with each other and must
@@ -295,7 +303,9 @@ sv_status sv_sample_accept(const float* logits, const float* draft_probs, int vo
  * s = ctx_lens[b] + j (page block_table[b, s / page_size], row
  * s % page_size) receives, for every KV head, the K and V of tree node
  * accepted_nodes[b, j] (a bit copy).  new_ctx_lens[b] = ctx_lens[b] +
- * accept_len[b] + 1 if non-NULL; it must not alias ctx_lens.  The caller
+ * accept_len[b] + 1 if non-NULL (ctx_lens[b] when accept_len[b] > max_depth,
+ * which commits nothing for b and records SV_DEVERR_DEPTH); it must not
+ * alias ctx_lens.  The caller
  * guarantees pages for slots L_b .. L_b + max_depth.  Nothing else changes.
  *
  * tree_k/tree_v: bf16 [num_layers][T, Hkv, D], layer stride

@@ -70,6 +70,19 @@ struct Params {
   bool vec4;
 };
 
+// Outputs of a sequence whose tree cannot be walked (no node, or more than
+// kMaxNodes): accept length 0, no bonus token (-1), a path of -1; the error
+// word records SV_DEVERR_BAD_TREE.  Called by every thread of a CTA.
+__device__ void write_no_tree(const Params& p, int b) {
+  int* out_path = p.accepted_nodes + static_cast<size_t>(b) * (p.max_depth + 1);
+  for (int d = threadIdx.x; d <= p.max_depth; d += blockDim.x) out_path[d] = -1;
+  if (threadIdx.x == 0) {
+    p.accept_len[b] = 0;
+    p.bonus[b] = -1;
+    report_error(p.err, SV_DEVERR_BAD_TREE);
+  }
+}
+
 // Tree walk of sequence b (nodes n0 .. n0 + N - 1) by the whole CTA, one node
 // per thread; `scratch` is 8 KB of shared memory nothing else uses now.
 __device__ void walk_sequence(const Params& p, int b, int n0, int N, uint8_t* scratch) {
@@ -83,10 +96,11 @@ __device__ void walk_sequence(const Params& p, int b, int n0, int N, uint8_t* sc
   int* s_best = reinterpret_cast<int*>(s_good + 4);
   const int t = threadIdx.x;
   if (N < 1 || N > kMaxNodes) {  // uniform over the CTA
-    if (t == 0) {
-      report_error(p.err, SV_DEVERR_BAD_TREE);
-      p.tickets[b] = 0;
-    }
+    // no walk: the keys go back to zero for the next call on this
+    // workspace, and the sequence gets defined outputs
+    for (int i = t; i < N; i += blockDim.x) p.keys[n0 + i] = 0ull;
+    write_no_tree(p, b);
+    if (t == 0) p.tickets[b] = 0;
     return;
   }
   if (t < 4) s_good[t] = 0u;
@@ -283,6 +297,24 @@ __global__ void __launch_bounds__(kThreads) greedy_accept_kernel(const __grid_co
     __threadfence();
     walk_sequence(p, s_b, s_n0, s_n, dyn);
   }
+  // A sequence without nodes owns no row, so no CTA above is its last one:
+  // the first CTA gives every such sequence its defined outputs.
+  if (blockIdx.x == 0 && blockIdx.y == 0) {
+    for (int b0 = 0; b0 < p.batch; b0 += kThreads) {
+      const int bb = b0 + threadIdx.x;
+      const bool empty = bb < p.batch && p.cu_nodes[bb + 1] - p.cu_nodes[bb] < 1;
+      const int n_empty = __syncthreads_count(empty);
+      if (n_empty == 0) continue;
+      __shared__ int s_empty[kThreads];
+      __shared__ int s_count;
+      if (threadIdx.x == 0) s_count = 0;
+      __syncthreads();
+      if (empty) s_empty[atomicAdd(&s_count, 1)] = bb;
+      __syncthreads();
+      for (int i = 0; i < n_empty; ++i) write_no_tree(p, s_empty[i]);
+      __syncthreads();
+    }
+  }
 }
 
 }  // namespace acc
@@ -357,24 +389,57 @@ constexpr size_t kStaticScratchBytes = kWorkspaceHeader + static_cast<size_t>(kS
 
 static __device__ __align__(256) unsigned char g_accept_scratch[kStaticScratchBytes];
 
+// Unique id (over the process) of the context current on this thread, 0 when
+// it cannot be read.  A cudaDeviceReset ends a device's primary context; the
+// next one gets a new id and this library's module is loaded into it afresh.
+unsigned long long current_context_id() {
+  using GetCurrentFn = CUresult (*)(CUcontext*);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static std::once_flag once;
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrentFn>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetIdFn>(fn);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
 // Device address of the scratch array on the current device.  The first call
-// on each device resolves it (with that device current) and caches it.
+// on each device resolves it (with that device current) and caches it with
+// the id of the device's context; a later call in another context of that
+// device (after a cudaDeviceReset) resolves it again.
 void* static_scratch(sv_status* st) {
   static std::mutex mu;
   static void* addr[64] = {nullptr};
+  static unsigned long long ctx_id[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
     *st = SV_ERR_CUDA;
     return nullptr;
   }
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
+  const unsigned long long id = current_context_id();
+  if (addr[dev] == nullptr || id == 0 || id != ctx_id[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_accept_scratch) != cudaSuccess || p == nullptr) {
       *st = SV_ERR_CUDA;
       return nullptr;
     }
     addr[dev] = p;
+    ctx_id[dev] = current_context_id();
   }
   *st = SV_OK;
   return addr[dev];

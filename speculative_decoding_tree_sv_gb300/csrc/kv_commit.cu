@@ -42,11 +42,15 @@ __global__ void __launch_bounds__(256) kv_commit_kernel(const __grid_constant__ 
   const int a = p.accept_len[b];
   if (j > a) return;
   const int L = p.ctx_lens[b];
-  if (j == 0 && layer == 0 && threadIdx.x == 0 && p.new_ctx_lens != nullptr) p.new_ctx_lens[b] = L + a + 1;
   if (a > p.max_depth) {
-    if (threadIdx.x == 0) report_error(p.err, SV_DEVERR_DEPTH);
+    // nothing of this sequence is committed, so its length stays L
+    if (threadIdx.x == 0) {
+      report_error(p.err, SV_DEVERR_DEPTH);
+      if (j == 0 && layer == 0 && p.new_ctx_lens != nullptr) p.new_ctx_lens[b] = L;
+    }
     return;
   }
+  if (j == 0 && layer == 0 && threadIdx.x == 0 && p.new_ctx_lens != nullptr) p.new_ctx_lens[b] = L + a + 1;
   const int n0 = p.cu_nodes[b];
   const int N = p.cu_nodes[b + 1] - n0;
   const int node = p.accepted_nodes[static_cast<size_t>(b) * (p.max_depth + 1) + j];

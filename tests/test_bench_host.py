@@ -40,3 +40,15 @@ def test_reference_arm_prints_one_contract_line():
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["config"]["workload"] == bench.WORKLOADS["llama8b_eagle"]
+    # whole steps are timed: the line's time is what the steps took
+    assert d["steps"] == 1 and "whole oracle steps" in d["cpu_baseline"]["sample"]
+
+
+def test_both_arms_print_the_same_config():
+    import bench
+    from synth import make_case
+    for name in ("llama8b_eagle", "tiny"):
+        case, _ = bench.build_case(name, with_logits=False)
+        cfg = bench.workload_config(name, case)
+        assert cfg["workload"] == bench.WORKLOADS[name]
+        assert set(cfg) == {"workload", "layers", "batch", "total_nodes", "seed", "l2", "parallelism"}

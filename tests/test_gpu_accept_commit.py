@@ -262,3 +262,103 @@ def test_commit_bad_path_is_reported():
     # slots 0 and 2 of the path were written, slot 1 was skipped
     changed = (before != dc.k_cache).any(dim=-1).any(dim=2).sum().item()
     assert changed == 2
+
+
+def _accept_call(case, cu_nodes, T, ws, max_depth=None):
+    dev = "cuda"
+    B, V = len(cu_nodes) - 1, case.vocab
+    md = case.max_depth if max_depth is None else max_depth
+    am = torch.full((T,), -7, dtype=torch.int32, device=dev)
+    alen = torch.full((B,), -7, dtype=torch.int32, device=dev)
+    anodes = torch.full((B, md + 1), -7, dtype=torch.int32, device=dev)
+    bonus = torch.full((B,), -7, dtype=torch.int32, device=dev)
+    binding.sv_greedy_accept(torch.from_numpy(case.logits[:T]).to(dev), V, i32(case.tokens[:T]),
+                             i32(case.parents[:T]), i32(cu_nodes), B, T, case.max_nodes, md, am, alen, anodes,
+                             bonus, ws)
+    torch.cuda.synchronize()
+    return dict(argmax=am.cpu().numpy(), accept_len=alen.cpu().numpy(), accepted_nodes=anodes.cpu().numpy(),
+                bonus=bonus.cpu().numpy(), err=binding.sv_get_device_error(ws))
+
+
+def test_empty_tree_in_a_batch_gets_defined_outputs():
+    """A sequence with no nodes owns no row of the grid; it still gets
+    accept_len 0, bonus -1 and a path of -1, the call reports a bad tree, and
+    the other sequences keep the oracle's answers."""
+    case = make_case("tiny", batch=3)
+    cu = case.cu_nodes.copy()
+    T = int(cu[2])
+    cu[3] = cu[2]  # the last sequence is empty
+    for empty_at in (2, 0):
+        cu_e = cu.copy()
+        if empty_at == 0:  # empty first sequence: its nodes are dropped at the front
+            n0 = int(case.cu_nodes[1])
+            sub = make_case("tiny", batch=3)
+            sub.logits, sub.tokens, sub.parents = case.logits[n0:], case.tokens[n0:], case.parents[n0:]
+            cu_e = np.concatenate([[0], case.cu_nodes[1:] - n0]).astype(np.int32)
+            src, Tn = sub, int(cu_e[-1])
+        else:
+            src, Tn = case, T
+        ws = torch.zeros(binding.sv_greedy_accept_workspace_size(3, Tn), dtype=torch.uint8, device="cuda")
+        res = _accept_call(src, cu_e, Tn, ws)
+        assert res["err"] == binding.SV_DEVERR_BAD_TREE
+        assert res["accept_len"][empty_at] == 0 and res["bonus"][empty_at] == -1
+        assert (res["accepted_nodes"][empty_at] == -1).all()
+        others = [b for b in range(3) if b != empty_at]
+        sub_cu = np.concatenate([[0], np.cumsum([cu_e[b + 1] - cu_e[b] for b in others])]).astype(np.int32)
+        ref = oracle.greedy_accept(src.logits[:Tn], src.tokens[:Tn], src.parents[:Tn], sub_cu)
+        for i, b in enumerate(others):
+            assert res["accept_len"][b] == ref["accept_len"][i]
+            assert res["bonus"][b] == ref["bonus"][i]
+            assert list(res["accepted_nodes"][b][: ref["accept_len"][i] + 1]) == ref["accepted_nodes"][i]
+        assert int(ws[256:].count_nonzero()) == 0  # keys and tickets reset
+
+
+def test_oversized_tree_resets_its_keys_and_gets_defined_outputs():
+    """A tree of more than 128 nodes (device cu_nodes disagreeing with the
+    host's max_nodes) is not walked: defined outputs, a bad-tree report, and
+    its arg-max keys return to zero, so the next call on the same workspace
+    is right."""
+    rng = np.random.default_rng(5)
+    T, V = 150, 4096
+    bad = _Tiny()
+    bad.vocab, bad.max_nodes, bad.max_depth = V, 128, 12
+    bad.logits = rng.standard_normal((T, V)).astype(np.float32)
+    bad.tokens = rng.integers(0, V, T).astype(np.int32)
+    bad.parents = np.concatenate([[-1], np.arange(T - 1)]).astype(np.int32)  # a chain of 140 ...
+    bad.parents[140:] = np.arange(-1, 9)  # ... then a chain of 10 (local ids) from index 140
+    cu_bad = np.array([0, 140, 150], np.int32)
+    ws = torch.zeros(binding.sv_greedy_accept_workspace_size(2, T), dtype=torch.uint8, device="cuda")
+    res = _accept_call(bad, cu_bad, T, ws)
+    assert res["err"] == binding.SV_DEVERR_BAD_TREE
+    assert res["accept_len"][0] == 0 and res["bonus"][0] == -1 and (res["accepted_nodes"][0] == -1).all()
+    ref = oracle.greedy_accept(bad.logits[140:], bad.tokens[140:], bad.parents[140:], np.array([0, 10], np.int32))
+    assert res["accept_len"][1] == ref["accept_len"][0] and res["bonus"][1] == ref["bonus"][0]
+    assert int(ws[256:].count_nonzero()) == 0
+    # the same workspace, a valid call
+    good = make_case("tiny", batch=2)
+    Tg = int(good.cu_nodes[-1])
+    assert Tg <= T
+    res2 = _accept_call(good, good.cu_nodes, Tg, ws)
+    _assert_accept_equal(res2, oracle.greedy_accept(good.logits, good.tokens, good.parents, good.cu_nodes), good)
+
+
+def test_commit_depth_error_keeps_the_length():
+    """accept_len beyond max_depth commits nothing for that sequence and
+    leaves its new length at L (cache and length agree)."""
+    case = make_case("tiny")
+    dc = DeviceCase(case)
+    T, Hkv, D = case.total_nodes, case.num_kv_heads, case.head_dim
+    md = case.max_depth
+    anodes = np.full((1, md + 1), -1, np.int32)
+    anodes[0, :2] = [0, 1]
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    new_lens = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    before_k, before_v = dc.k_cache.clone(), dc.v_cache.clone()
+    binding.sv_kv_commit(dc.tree_k, dc.tree_v, T * Hkv * D, dc.k_cache, dc.v_cache,
+                         case.num_pages * Hkv * 16 * D, 1, case.num_pages, dc.block_table,
+                         case.max_pages_per_seq, dc.ctx_lens, dc.cu_nodes, i32(anodes), i32([md + 1]), 1,
+                         md, Hkv, D, 16, new_lens, ws)
+    torch.cuda.synchronize()
+    assert binding.sv_get_device_error(ws) == binding.SV_DEVERR_DEPTH
+    assert int(new_lens.item()) == int(case.ctx_lens[0])
+    assert torch.equal(before_k, dc.k_cache) and torch.equal(before_v, dc.v_cache)
