@@ -11,7 +11,9 @@ verification hot path computes, written from the method descriptions:
 * ``commit``     — the KV cache after the accepted path is written to slots
   L .. L + a.
 * ``retrieval``  — SpecPV block retrieval: max/min key summaries of 16-token
-  pages, block importance against the tree's queries, the partial page list.
+  pages, block importance against the tree's queries, the partial page list;
+  the full/partial schedule and the tree of a full verification that
+  re-verifies the buffer of partially verified tokens.
 * ``sampling``   — stochastic (temperature > 0) acceptance: speculative
   sampling node by node over the tree, residual draws for the bonus token.
 
@@ -43,4 +45,6 @@ from .retrieval import (  # noqa: F401
     page_summaries,
     query_block_score,
     retrieve_pages,
+    specpv_full_step_trees,
+    specpv_full_tree,
 )

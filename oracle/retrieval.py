@@ -176,3 +176,62 @@ def specpv_schedule(step_commits: Sequence[int], step_tokens: int, buffer_limit:
             kinds.append("partial")
             ctx += int(c)
     return kinds
+
+
+def specpv_full_tree(cand_parents: Sequence[int], cand_tokens: Sequence[int],
+                     buffer_tokens: Sequence[int]) -> Tuple[np.ndarray, np.ndarray]:
+    """The tree of a full verification that follows partial ones, for one
+    sequence (SpecPV section 3.3, "Rectified with Full Verification": before
+    the full verification, the partially verified tokens are prepended to the
+    new candidates; the full KV cache is used and the partial cache is
+    refreshed).
+
+    ``buffer_tokens`` are the tokens committed since the last full
+    verification, in order: positions R .. L-1, R being the context length at
+    that refresh.  ``cand_parents`` / ``cand_tokens`` are this step's
+    candidate tree (sequence-local ids, root = node 0 = the last accepted
+    token, at position L).  The result puts the buffered tokens in a chain
+    from the root (node j is the token at position R + j, its parent j - 1)
+    and hangs the candidate tree below the chain's last node: candidate node
+    i becomes node nb + i (nb = number of buffered tokens), with parent
+    nb + parent[i], and the candidate root's parent is nb - 1.  Reading of
+    the pages: the step is verified at context length R, so every buffered
+    token is checked again like a candidate (node j is accepted when its
+    token is the target's choice after node j - 1), and the commit writes
+    slots R .. R + a, rewriting the buffered slots with the K/V of this
+    forward.  With no buffered token the result is the candidate tree.
+
+    Returns (parents int32 [nb + N], tokens int32 [nb + N])."""
+    nb = len(buffer_tokens)
+    n = len(cand_parents)
+    parents = np.empty(nb + n, dtype=np.int32)
+    tokens = np.empty(nb + n, dtype=np.int32)
+    for j in range(nb):
+        parents[j] = j - 1
+        tokens[j] = int(buffer_tokens[j])
+    for i in range(n):
+        if i == 0:
+            parents[nb] = nb - 1  # -1 when nothing is buffered
+        else:
+            parents[nb + i] = nb + int(cand_parents[i])
+        tokens[nb + i] = int(cand_tokens[i])
+    return parents, tokens
+
+
+def specpv_full_step_trees(cand_parents: Sequence[int], cand_tokens: Sequence[int], cand_cu: Sequence[int],
+                           buffer_tokens: Sequence[int], buffer_cu: Sequence[int]
+                           ) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """specpv_full_tree for every sequence of a batch: candidate trees packed
+    with offsets cand_cu [B+1], buffered tokens packed with offsets
+    buffer_cu [B+1].  Returns (parents, tokens, cu_nodes) of the combined
+    trees, packed in sequence order."""
+    par_all, tok_all, cu = [], [], [0]
+    for b in range(len(cand_cu) - 1):
+        c0, c1 = int(cand_cu[b]), int(cand_cu[b + 1])
+        b0, b1 = int(buffer_cu[b]), int(buffer_cu[b + 1])
+        par, tok = specpv_full_tree(cand_parents[c0:c1], cand_tokens[c0:c1], buffer_tokens[b0:b1])
+        par_all.append(par)
+        tok_all.append(tok)
+        cu.append(cu[-1] + len(par))
+    cat = (lambda xs: np.concatenate(xs).astype(np.int32)) if par_all else (lambda xs: np.zeros(0, np.int32))
+    return cat(par_all), cat(tok_all), np.asarray(cu, dtype=np.int32)

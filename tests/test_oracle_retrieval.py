@@ -179,3 +179,161 @@ def test_extended_lists_append_the_buffer_pages():
     # sequence 0: pages 0..10 at the refresh (last page 10), now 13 pages
     assert kv[cu[0]:cu[1]].tolist() == [0, 5, 9, 10, 11, 12]
     assert kv[cu[1]:cu[2]].tolist() == [1, 2]
+
+
+# ------------------------------------------------------------ SpecPV full step
+# SpecPV section 3.3: before a full verification, the partially verified
+# tokens are prepended to the new candidates and the full KV cache is used.
+
+def _rand_tree(rng, n):
+    from synth import tree_random_depth
+    return tree_random_depth(rng, n, min(4, n - 1)) if n > 1 else np.array([-1], np.int32)
+
+
+def test_full_tree_without_buffer_is_the_candidate_tree():
+    rng = np.random.default_rng(3)
+    for n in (1, 2, 9, 16):
+        par = _rand_tree(rng, n)
+        tok = rng.integers(0, 1000, n).astype(np.int32)
+        p2, t2 = oracle.specpv_full_tree(par, tok, [])
+        np.testing.assert_array_equal(p2, par)
+        np.testing.assert_array_equal(t2, tok)
+
+
+def test_full_tree_layout_by_hand():
+    # candidate tree 0 -> {1, 2}, 1 -> {3}; buffered tokens 11, 12, 13
+    par, tok = oracle.specpv_full_tree([-1, 0, 0, 1], [5, 6, 7, 8], [11, 12, 13])
+    assert par.tolist() == [-1, 0, 1, 2, 3, 3, 4]
+    assert tok.tolist() == [11, 12, 13, 5, 6, 7, 8]
+    par, tok, cu = oracle.specpv_full_step_trees([-1, 0, -1, 0, 0], [1, 2, 3, 4, 5], [0, 2, 5], [9, 8, 7], [0, 1, 3])
+    assert cu.tolist() == [0, 3, 8]
+    assert par.tolist() == [-1, 0, 1, -1, 0, 1, 2, 2]
+    assert tok.tolist() == [9, 1, 2, 8, 7, 3, 4, 5]
+
+
+@pytest.mark.parametrize("R,nb,n", [(40, 5, 9), (0, 3, 6), (17, 1, 1), (33, 12, 16)])
+def test_full_step_attention_chain_is_causal_and_candidates_see_the_buffer(R, nb, n):
+    """Rows of the chain (buffered tokens and the step's root) equal causal
+    attention over the context and the chain (torch SDPA); a candidate row
+    sees the context, the whole chain and its own ancestors."""
+    from tests.test_oracle_attention import _sdpa, _single_seq
+    rng = np.random.default_rng(R * 100 + nb * 10 + n)
+    cand = _rand_tree(rng, n)
+    par, _ = oracle.specpv_full_tree(cand, np.zeros(n, np.int32), np.zeros(nb, np.int32))
+    d = _single_seq(rng, R, par, 8, 2, 32)
+    out, _ = oracle.tree_verify_attention(d["q"], d["tree_k"], d["tree_v"], d["k_cache"], d["v_cache"],
+                                          d["block_table"], d["ctx_lens"], d["cu_nodes"], d["parents"])
+    m = nb + n
+    allowed = np.zeros((m, R + m), dtype=bool)
+    allowed[:, :R] = True
+    for i in range(nb + 1):  # chain rows: causal, bottom-right aligned
+        allowed[i, R: R + i + 1] = True
+    for i in range(1, n):  # candidate rows: the chain, then their own ancestors
+        row = nb + i
+        allowed[row, R: R + nb + 1] = True
+        j = i
+        while j != 0:
+            allowed[row, R + nb + j] = True
+            j = int(cand[j])
+    np.testing.assert_allclose(out, _sdpa(d, allowed), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("R,nb,n", [(48, 7, 12), (5, 2, 3), (64, 20, 30)])
+def test_full_step_with_unchanged_buffer_kv_equals_full_verification(R, nb, n):
+    """If the buffered tokens' K/V in the cache were already exact, re-verifying
+    them changes nothing: the candidate rows of the combined step at context
+    length R equal plain full verification of the candidate tree at L = R + nb
+    over a cache holding the chain's K/V in slots R .. L-1."""
+    from tests.test_oracle_attention import _paged, _rand_bf16
+    rng = np.random.default_rng(R + nb + n)
+    Hq, Hkv, D = 8, 2, 32
+    cand = _rand_tree(rng, n)
+    par, _ = oracle.specpv_full_tree(cand, np.zeros(n, np.int32), np.zeros(nb, np.int32))
+    m = nb + n
+    L = R + nb
+    kc = _rand_bf16(rng, (L, Hkv, D))
+    vc = _rand_bf16(rng, (L, Hkv, D))
+    q = _rand_bf16(rng, (m, Hq, D))
+    tk = _rand_bf16(rng, (m, Hkv, D))
+    tv = _rand_bf16(rng, (m, Hkv, D))
+    tk[:nb], tv[:nb] = kc[R:], vc[R:]  # the chain's K/V = what the cache holds there
+    kcache, table = _paged(rng, kc, m + 2)
+    vcache = kcache.copy()
+    for t in range(L):
+        vcache[table[t // 16], :, t % 16, :] = vc[t]
+    bt = table[None, :]
+    combined, _ = oracle.tree_verify_attention(q, tk, tv, kcache, vcache, bt, np.array([R], np.int32),
+                                               np.array([0, m], np.int32), par)
+    plain, _ = oracle.tree_verify_attention(q[nb:], tk[nb:], tv[nb:], kcache, vcache, bt, np.array([L], np.int32),
+                                            np.array([0, n], np.int32), cand)
+    np.testing.assert_allclose(combined[nb:], plain, rtol=0, atol=1e-12)
+
+
+def _plant(logits, node, token):
+    logits[node, :] = 0.0
+    logits[node, token] = 5.0
+
+
+def test_full_step_acceptance_rechecks_the_buffer():
+    """Greedy acceptance over the combined tree: a buffer the target agrees
+    with is accepted again and the walk continues into the candidates; a
+    buffered token the target now rejects ends the path there, with the
+    target's own token as the bonus."""
+    rng = np.random.default_rng(8)
+    V, nb = 64, 5
+    cand = np.array([-1, 0, 0, 1, 1, 2], np.int32)
+    cand_tok = np.array([0, 10, 11, 12, 13, 14], np.int32)
+    buf = np.array([40, 41, 42, 43, 44], np.int32)
+    par, tok = oracle.specpv_full_tree(cand, cand_tok, buf)
+    m = len(par)
+    cu = np.array([0, m], np.int32)
+    logits = rng.standard_normal((m, V))
+    # chain agrees: am[j] = token of node j + 1 along the chain and into the
+    # candidate root's child 1 (token 10), then child 3 (token 12)
+    for j in range(nb - 1):
+        _plant(logits, j, buf[j + 1])
+    _plant(logits, nb - 1, cand_tok[0])  # the step's root token follows the buffer
+    _plant(logits, nb, 10)
+    _plant(logits, nb + 1, 12)
+    _plant(logits, nb + 3, 63)  # no child carries 63: the walk stops at node nb + 3
+    for i in (nb + 2, nb + 4, nb + 5):
+        _plant(logits, i, 62)
+    acc = oracle.greedy_accept(logits, tok, par, cu)
+    assert acc["accept_len"][0] == nb + 2
+    assert acc["accepted_nodes"][0] == list(range(nb + 1)) + [nb + 1, nb + 3]
+    assert acc["bonus"][0] == 63
+    # the target disagrees with buffered token 3 (node 3): the path ends at node 2
+    _plant(logits, 2, 7)
+    acc = oracle.greedy_accept(logits, tok, par, cu)
+    assert acc["accept_len"][0] == 2 and acc["accepted_nodes"][0] == [0, 1, 2] and acc["bonus"][0] == 7
+
+
+def test_full_step_commit_rewrites_the_buffered_slots():
+    """The commit of the combined step at context length R writes slots
+    R .. R + a: the buffered slots get this forward's K/V, the accepted
+    candidates follow, and the new length is L + a_cand + 1 when the whole
+    buffer is accepted again."""
+    rng = np.random.default_rng(12)
+    Hkv, D, R, nb = 2, 8, 30, 4
+    L = R + nb
+    cand = np.array([-1, 0, 1, 0], np.int32)
+    par, _ = oracle.specpv_full_tree(cand, np.zeros(4, np.int32), np.zeros(nb, np.int32))
+    m = len(par)
+    pages = 4
+    k_cache = rng.integers(0, 1 << 16, (1, pages, Hkv, 16, D)).astype(np.uint16)
+    v_cache = rng.integers(0, 1 << 16, (1, pages, Hkv, 16, D)).astype(np.uint16)
+    tk = rng.integers(0, 1 << 16, (1, m, Hkv, D)).astype(np.uint16)
+    tv = rng.integers(0, 1 << 16, (1, m, Hkv, D)).astype(np.uint16)
+    bt = np.array([[2, 0, 3, 1]], np.int32)
+    path = list(range(nb + 1)) + [nb + 1, nb + 2]  # the buffer, the root, two candidates
+    a = len(path) - 1
+    k2, v2, lens = oracle.kv_commit(k_cache, v_cache, tk, tv, bt, np.array([R], np.int32),
+                                    np.array([0, m], np.int32), [path], [a], 16)
+    assert int(lens[0]) == L + 2 + 1
+    for j, node in enumerate(path):
+        s = R + j
+        np.testing.assert_array_equal(k2[0, bt[0, s // 16], :, s % 16], tk[0, node])
+        np.testing.assert_array_equal(v2[0, bt[0, s // 16], :, s % 16], tv[0, node])
+    untouched = [s for s in range(pages * 16) if not R <= s <= R + a]
+    for s in untouched:
+        np.testing.assert_array_equal(k2[0, bt[0, s // 16], :, s % 16], k_cache[0, bt[0, s // 16], :, s % 16])
