@@ -57,6 +57,7 @@ WORKLOADS = {
     "long_partial_pv": "60000-token context, 48-node tree, SpecPV partial list (64 sink + 32x64 retrieved + last 1024)",
     "specblock": "SpecBlock trees (<=128 nodes, depth <=12), batch 16, 64 q / 8 kv heads, context 16384",
 }
+KERNEL_NAMES = ["paired 128-row CTAs", "256-row CTAs", "256-row CTAs, work dealt evenly over one CTA per SM"]
 # one attention layer of each of these is timed next to the headline step
 PER_CONFIG = ("tiny", "serving_mix", "long_partial", "long_partial_pv", "specblock")
 # (sequence, KV head) units of the SpecBlock layer the oracle times; the
@@ -276,7 +277,7 @@ class GpuStep:
         self.new_lens = torch.empty(B, dtype=torch.int32, device=dev)
 
     def launches_per_step(self):
-        per_attn = 2 if self.split_reduce == 2 else 1
+        per_attn = 2 if (self.split_reduce == 2 or self.kernel == 2) else 1  # + the split or dealt combine
         return self.layers * per_attn + 2
 
     def attention_all_layers(self):
@@ -557,7 +558,7 @@ class AttentionLeg:
     `replicas` times (distinct addresses) so the calls of one replay read
     more than twice the L2 from HBM."""
 
-    def __init__(self, torch, case, partial, dev, bytes_per_call):
+    def __init__(self, torch, case, partial, dev, bytes_per_call, flags: int = 0):
         from speculative_decoding_tree_sv_gb300 import binding
         self.torch, self.binding, self.case, self.partial = torch, binding, case, partial
         c = case
@@ -595,7 +596,7 @@ class AttentionLeg:
                 v_cache=self.v_cache[r], block_table=self.block_table, ctx_lens=self.ctx_lens,
                 cu_nodes=self.cu_nodes, parents=self.parents, out=self.out[r], total_nodes=c.total_nodes,
                 max_nodes=c.max_nodes, kv_pages=self.kv_pages, cu_kv_pages=self.cu_kv_pages,
-                max_kv_pages=max_kv)
+                max_kv_pages=max_kv, flags=flags)
             ws_bytes = max(ws_bytes, binding.sv_tree_attention_workspace_size(p))
             self.params.append(p)
         self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
@@ -608,7 +609,7 @@ class AttentionLeg:
             self.binding.sv_tree_attention(p)
 
     def launches(self):
-        return self.replicas * (2 if self.split_reduce == 2 else 1)
+        return self.replicas * (2 if (self.split_reduce == 2 or self.kernel == 2) else 1)
 
 
 def per_config_leg(torch, name, args, dev, peaks):
@@ -626,7 +627,7 @@ def per_config_leg(torch, name, args, dev, peaks):
     roof = attention_roofline(case, partial, us, peak, peak_kind, tpeak, tpeak_kind, measured_traffic(name))
     nodes = case.total_nodes
     out = {"workload": WORKLOADS[name], "us_per_call": us, "nodes_per_s_per_layer": nodes / (us * 1e-6),
-           "roofline": roof, "kernel": ["paired 128-row CTAs", "256-row CTAs"][leg.kernel],
+           "roofline": roof, "kernel": KERNEL_NAMES[leg.kernel],
            "kv_splits": leg.splits, "layer_copies": leg.replicas,
            "gpu_launches": leg.launches() * args.steps}
     if not args.no_cpu_baseline:
@@ -809,8 +810,8 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(args.config, c),
-        "plan": {"kv_splits": st.splits, "split_merge": "combine kernel" if st.split_reduce == 2 else "none",
-                 "attention_kernel": ["paired 128-row CTAs", "256-row CTAs"][st.kernel], "cuda_graph": True,
+        "plan": {"kv_splits": st.splits, "split_merge": "combine kernel" if (st.split_reduce == 2 or st.kernel == 2) else "none",
+                 "attention_kernel": KERNEL_NAMES[st.kernel], "cuda_graph": True,
                  "early_context": bool(flags)},
         "roofline": roofline,
         "cpu_baseline": cpu,

@@ -33,7 +33,8 @@
  *     unsupported.
  *   - A workspace must be zero-filled once after allocation (for example with
  *     cudaMemset) and must not be shared by calls that may run concurrently.
- *     Each call leaves its workspace ready for the next call.
+ *     Each call leaves its workspace ready for the next call; after a call
+ *     that reported a device error or a timeout, zero it again.
  *   - Symbols are thread-safe; per-stream ordering is the caller's.
  */
 #ifndef SV_H_
@@ -113,9 +114,14 @@ enum sv_attn_flags {
    * CTA per 128-row tile, the two row tiles of a group share each K/V tile
    * by cluster multicast, scores double-buffered in TMEM; suits short
    * contexts split across many CTAs.  WIDE: one CTA per 256-row group, each
-   * K/V tile staged in one SM only; suits long and batched contexts. */
+   * K/V tile staged in one SM only, the context split evenly per group.
+   * DEALT: the WIDE engine in one CTA per SM, the call's whole work (every
+   * sequence, KV head and row group, weighted by 128-row tiles) dealt to
+   * the CTAs in equal contiguous ranges, so batches of uneven or many
+   * sequences run in one even wave; suits long and batched contexts. */
   SV_ATTN_KERNEL_PAIRED = 2,
-  SV_ATTN_KERNEL_WIDE = 4
+  SV_ATTN_KERNEL_WIDE = 4,
+  SV_ATTN_KERNEL_DEALT = 8
 };
 
 typedef struct sv_attn_params {
@@ -130,7 +136,10 @@ typedef struct sv_attn_params {
   int max_nodes;          /* max_b N_b (host copy), 1..128                   */
   int max_pages_per_seq;  /* row length of block_table                       */
   int max_kv_pages;       /* partial mode: max_b listed pages (host copy)    */
-  int num_splits;         /* KV splits per (sequence, head group); 0 = auto  */
+  int num_splits;         /* KV splits per (sequence, head group); 0 = auto
+                             (a count > 0 selects a split kernel, paired or
+                             wide, unless SV_ATTN_KERNEL_DEALT is set; the
+                             dealt kernel ignores it)                        */
   int split_reduce;       /* how splits merge: 0 = auto, 2 = through
                              workspace partials and a combine kernel (the
                              only merge; other values are rejected)          */
@@ -166,7 +175,9 @@ sv_status sv_tree_attention_workspace_size(const sv_attn_params* params, size_t*
 /* The launch plan sv_tree_attention would use for these parameters: the
  * number of KV splits, how they merge (0 = single split, 2 = through
  * workspace partials and the combine kernel) and, if kernel is non-NULL,
- * the kernel (0 = paired, 1 = wide; see sv_attn_flags). */
+ * the kernel (0 = paired, 1 = wide, 2 = dealt; see sv_attn_flags).  For the
+ * dealt kernel num_splits is 1 and split_reduce 0: its own combine merges the
+ * units that its ranges cut. */
 sv_status sv_tree_attention_plan(const sv_attn_params* params, int* num_splits, int* split_reduce, int* kernel);
 
 /* Launches the attention (and, with more than one split, the split combine)
@@ -443,6 +454,39 @@ sv_status sv_specpv_after(sv_specpv_seq* seq, sv_verify_kind kind, int ctx_len_a
 sv_status sv_partial_list_extend(const int* ref_pages, const int* ref_cu, const int* ref_ctx_lens,
                                  const int* ctx_lens, int batch, int* kv_pages, int* cu_kv_pages,
                                  void* workspace, size_t workspace_bytes, sv_stream_t stream);
+
+/* The trees of a full verification that follows partial ones (SpecPV
+ * section 3.3: before a full verification, the partially verified tokens are
+ * prepended to the new candidates; the full KV cache is used).
+ *
+ * Per sequence b: the buffered tokens buffer_tokens[buffer_cu[b] ..
+ * buffer_cu[b+1]) (the nb tokens committed since the last full
+ * verification, positions R .. L-1 with R = refresh_ctx_len) and the
+ * candidate tree (cand_parents / cand_tokens [cand_cu[b] .. cand_cu[b+1]),
+ * local ids, root = the last accepted token at position L).  Output, packed
+ * in sequence order with prefix sums cu_nodes [B+1]: node j < nb is buffered
+ * token j with parent j - 1 (the chain's first node is the root), node
+ * nb + i is candidate node i with parent nb + cand_parents[i], and the
+ * candidate root's parent is nb - 1 (-1 when nb = 0: the candidate tree
+ * unchanged).
+ *
+ * The full step then runs sv_tree_attention, sv_greedy_accept and
+ * sv_kv_commit on these trees with ctx_lens = R (full KV): every buffered
+ * token is checked again like a candidate (node j is accepted when its token
+ * is the target's arg-max after node j - 1; a rejection ends the path there
+ * and the bonus token replaces the buffered one), and the commit writes slots
+ * R .. R + a, rewriting the buffered slots with this forward's K/V.  The
+ * caller's host sizes: total_nodes = total candidate nodes + sum nb;
+ * max_nodes = max(nb + candidate nodes) <= 128; max_depth = max(nb +
+ * candidate depth).  Device errors: a sequence with nb < 0, no candidate
+ * node or more than 128 combined nodes -> SV_DEVERR_BAD_TREE; a candidate
+ * parent not before its child -> SV_DEVERR_BAD_PARENT (the tree is still
+ * written).  parents/tokens need room for all combined nodes; buffer_tokens
+ * may be NULL when every buffer is empty; workspace optional (error word). */
+sv_status sv_specpv_full_trees(const int* cand_parents, const int* cand_tokens, const int* cand_cu,
+                               const int* buffer_tokens, const int* buffer_cu, int batch,
+                               int* parents, int* tokens, int* cu_nodes, void* workspace,
+                               size_t workspace_bytes, sv_stream_t stream);
 
 /* Diagnostics: per-CTA phase tracing of sv_tree_attention.
  *

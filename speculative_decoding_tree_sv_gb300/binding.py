@@ -26,6 +26,7 @@ SV_DEVERR_BAD_PATH, SV_DEVERR_DEPTH, SV_DEVERR_BAD_TREE = 4, 5, 6
 SV_ATTN_EARLY_CONTEXT = 1
 SV_ATTN_KERNEL_PAIRED = 2
 SV_ATTN_KERNEL_WIDE = 4
+SV_ATTN_KERNEL_DEALT = 8
 DEVICE_ERRORS = {0: "none", 1: "timeout", 2: "bad parent", 3: "bad page", 4: "bad path", 5: "depth",
                  6: "bad tree"}
 
@@ -123,6 +124,9 @@ def load(path: Optional[str] = None):
     lib.sv_partial_list_extend.restype = c_int
     lib.sv_partial_list_extend.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p,
                                            c_void_p, c_size_t, c_void_p]
+    lib.sv_specpv_full_trees.restype = c_int
+    lib.sv_specpv_full_trees.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p,
+                                         c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
     lib.sv_specpv_next.restype = c_int
     lib.sv_specpv_next.argtypes = [P(sv_specpv_seq), c_int, c_int]
     lib.sv_specpv_after.restype = c_int
@@ -214,7 +218,7 @@ def sv_tree_attention_workspace_size(params: sv_attn_params) -> int:
 
 def sv_tree_attention_plan(params: sv_attn_params, with_kernel: bool = False):
     """(num_splits, split_reduce) the library would launch with, plus the
-    kernel (0 = paired, 1 = wide) when with_kernel is set."""
+    kernel (0 = paired, 1 = wide, 2 = dealt) when with_kernel is set."""
     s, m, k = c_int(0), c_int(0), c_int(0)
     _check(load().sv_tree_attention_plan(ctypes.byref(params), ctypes.byref(s), ctypes.byref(m), ctypes.byref(k)),
            "sv_tree_attention_plan")
@@ -356,6 +360,15 @@ def sv_partial_list_extend(ref_pages, ref_cu, ref_ctx_lens, ctx_lens, batch: int
     _check(load().sv_partial_list_extend(_ptr(ref_pages), _ptr(ref_cu), _ptr(ref_ctx_lens), _ptr(ctx_lens), batch,
                                          _ptr(kv_pages), _ptr(cu_kv_pages), _ptr(workspace), workspace_bytes,
                                          _stream(stream)), "sv_partial_list_extend")
+
+
+def sv_specpv_full_trees(cand_parents, cand_tokens, cand_cu, buffer_tokens, buffer_cu, batch: int, parents,
+                         tokens, cu_nodes, workspace=None, workspace_bytes: int = 0, stream=None) -> None:
+    if workspace is not None and not workspace_bytes:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(load().sv_specpv_full_trees(_ptr(cand_parents), _ptr(cand_tokens), _ptr(cand_cu), _ptr(buffer_tokens),
+                                       _ptr(buffer_cu), batch, _ptr(parents), _ptr(tokens), _ptr(cu_nodes),
+                                       _ptr(workspace), workspace_bytes, _stream(stream)), "sv_specpv_full_trees")
 
 
 def sv_specpv_next(seq: sv_specpv_seq, step_tokens: int, buffer_limit: int) -> int:

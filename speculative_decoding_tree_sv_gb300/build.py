@@ -18,8 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 LIBDIR = os.path.join(PKG, "lib")
 LIBNAME = "libsv.so"
-SOURCES = ["abi.cu", "tree_attention.cu", "tree_attention_wide.cu", "greedy_accept.cu", "sample_accept.cu", "kv_commit.cu",
-           "retrieval.cu"]
+SOURCES = ["abi.cu", "tree_attention.cu", "tree_attention_wide.cu", "tree_attention_dealt.cu", "greedy_accept.cu",
+           "sample_accept.cu", "kv_commit.cu", "retrieval.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -559,6 +559,65 @@ __global__ void __launch_bounds__(256) list_extend_kernel(const __grid_constant_
   }
 }
 
+// SpecPV section 3.3: before a full verification the partially verified
+// tokens are prepended to the new candidates.  One CTA per sequence b writes
+// its combined tree at the offset sum over earlier sequences of (buffered +
+// candidate nodes): the buffered tokens as a chain from the root (node j,
+// parent j - 1), then the candidate tree with ids shifted by the buffer's
+// length, its root's parent being the last buffered token.
+struct FullTreeParams {
+  const int* cand_parents;
+  const int* cand_tokens;
+  const int* cand_cu;
+  const int* buffer_tokens;
+  const int* buffer_cu;
+  int* parents;
+  int* tokens;
+  int* cu_nodes;
+  int* err;
+};
+
+__device__ __forceinline__ int combined_nodes(const FullTreeParams& p, int b) {
+  return max(0, p.buffer_cu[b + 1] - p.buffer_cu[b]) + max(0, p.cand_cu[b + 1] - p.cand_cu[b]);
+}
+
+__global__ void __launch_bounds__(256) full_tree_kernel(const __grid_constant__ FullTreeParams p) {
+  __shared__ int red[256];
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x;
+  int part = 0;
+  for (int j = tid; j < b; j += blockDim.x) part += combined_nodes(p, j);
+  red[tid] = part;
+  __syncthreads();
+  for (int s = blockDim.x / 2; s > 0; s >>= 1) {
+    if (tid < s) red[tid] += red[tid + s];
+    __syncthreads();
+  }
+  const int offset = red[0];
+  const int b0 = p.buffer_cu[b], nb = p.buffer_cu[b + 1] - b0;
+  const int c0 = p.cand_cu[b], n = p.cand_cu[b + 1] - c0;
+  if (tid == 0 && (nb < 0 || n < 1 || max(0, nb) + n > kMaxNodes)) report_error(p.err, SV_DEVERR_BAD_TREE);
+  const int nbv = max(0, nb), nv = max(0, n);
+  for (int j = tid; j < nbv; j += blockDim.x) {
+    p.parents[offset + j] = j - 1;
+    p.tokens[offset + j] = p.buffer_tokens[b0 + j];
+  }
+  for (int i = tid; i < nv; i += blockDim.x) {
+    int par = nbv - 1;  // the candidate root hangs below the chain (-1: no buffer)
+    if (i > 0) {
+      const int cp = p.cand_parents[c0 + i];
+      if (cp < 0 || cp >= i) report_error(p.err, SV_DEVERR_BAD_PARENT);
+      par = nbv + cp;
+    }
+    p.parents[offset + nbv + i] = par;
+    p.tokens[offset + nbv + i] = p.cand_tokens[c0 + i];
+  }
+  if (tid == 0) {
+    p.cu_nodes[b + 1] = offset + nbv + nv;
+    if (b == 0) p.cu_nodes[0] = 0;
+  }
+}
+
 }  // namespace retr
 }  // namespace sv
 
@@ -580,6 +639,29 @@ sv_status sv_partial_list_extend(const int* ref_pages, const int* ref_cu, const 
   p.cu_kv_pages = cu_kv_pages;
   p.err = static_cast<int*>(workspace);
   retr::list_extend_kernel<<<batch, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+sv_status sv_specpv_full_trees(const int* cand_parents, const int* cand_tokens, const int* cand_cu,
+                               const int* buffer_tokens, const int* buffer_cu, int batch, int* parents,
+                               int* tokens, int* cu_nodes, void* workspace, size_t workspace_bytes,
+                               sv_stream_t stream) {
+  using namespace sv;
+  if (!cand_parents || !cand_tokens || !cand_cu || !buffer_cu || !parents || !tokens || !cu_nodes || batch < 1)
+    return SV_ERR_INVALID_ARG;
+  if (workspace != nullptr && workspace_bytes < kWorkspaceHeader) return SV_ERR_WORKSPACE;
+  if (batch > 65535) return SV_ERR_UNSUPPORTED;
+  retr::FullTreeParams p;
+  p.cand_parents = cand_parents;
+  p.cand_tokens = cand_tokens;
+  p.cand_cu = cand_cu;
+  p.buffer_tokens = buffer_tokens;
+  p.buffer_cu = buffer_cu;
+  p.parents = parents;
+  p.tokens = tokens;
+  p.cu_nodes = cu_nodes;
+  p.err = static_cast<int*>(workspace);
+  retr::full_tree_kernel<<<batch, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
   return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 

@@ -47,4 +47,21 @@ struct WideLaunch {
 };
 sv_status launch_wide_attention(const sv_attn_params* p, const WideLaunch& w, cudaStream_t stream);
 
+// The evenly dealt 256-row kernel (tree_attention_dealt.cu): `ctas` resident
+// CTAs share the call's weighted (unit, tile) list in equal ranges; pieces of
+// units cut by a range boundary go to part_o / part_lse ([ctas][2][256 rows])
+// and the last piece of a unit to finish merges them; counters ([units][2],
+// zero between calls) count the finished pieces.
+struct DealtLaunch {
+  int ctas;
+  void* part_o;
+  float* part_lse;
+  int* counters;
+  int* err;
+  unsigned long long* trace;
+  long long trace_ctas;
+};
+size_t dealt_workspace_bytes(int ctas, int head_dim, long long units);
+sv_status launch_dealt_attention(const sv_attn_params* p, const DealtLaunch& w, cudaStream_t stream);
+
 }  // namespace sv

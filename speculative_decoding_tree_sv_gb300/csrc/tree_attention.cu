@@ -813,9 +813,10 @@ struct Plan {
   int group;
   int row_tiles;
   int paired;
-  int wide;  // 1: the 256-row kernel (tree_attention_wide.cu)
+  int wide;  // 1: the 256-row kernel (tree_attention_wide.cu), 2: the dealt one (tree_attention_dealt.cu)
   int splits;
   int mode;
+  int ctas;  // dealt kernel: resident CTAs
   size_t workspace;
 };
 
@@ -824,9 +825,13 @@ sv_status validate(const sv_attn_params* p) {
   if (p->batch < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1 || p->total_nodes < 0 || p->max_nodes < 1 ||
       p->max_pages_per_seq < 1 || p->num_pages < 1 || p->num_splits < 0 || p->max_kv_pages < 0 ||
       (p->split_reduce != 0 && p->split_reduce != 2) ||
-      (p->flags & ~static_cast<int>(SV_ATTN_EARLY_CONTEXT | SV_ATTN_KERNEL_PAIRED | SV_ATTN_KERNEL_WIDE)) != 0 ||
-      ((p->flags & SV_ATTN_KERNEL_PAIRED) && (p->flags & SV_ATTN_KERNEL_WIDE)))
+      (p->flags & ~static_cast<int>(SV_ATTN_EARLY_CONTEXT | SV_ATTN_KERNEL_PAIRED | SV_ATTN_KERNEL_WIDE |
+                                     SV_ATTN_KERNEL_DEALT)) != 0)
     return SV_ERR_INVALID_ARG;
+  {
+    const int k = p->flags & (SV_ATTN_KERNEL_PAIRED | SV_ATTN_KERNEL_WIDE | SV_ATTN_KERNEL_DEALT);
+    if ((k & (k - 1)) != 0) return SV_ERR_INVALID_ARG;  // at most one kernel forced
+  }
   if (p->num_q_heads % p->num_kv_heads != 0) return SV_ERR_INVALID_ARG;
   const int G = p->num_q_heads / p->num_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return SV_ERR_UNSUPPORTED;
@@ -951,6 +956,11 @@ int best_splits(const KernelCost& k, int tiles, int fixed_splits, double* cost) 
   return best_s;
 }
 
+// (sequence, KV head, 256-row group) slots of the dealt kernel's counters.
+long long dealt_units(const sv_attn_params* p, int group) {
+  return static_cast<long long>(p->batch) * p->num_kv_heads * ((static_cast<long long>(p->max_nodes) * group + 255) / 256);
+}
+
 sv_status make_plan(const sv_attn_params* p, Plan* plan) {
   sv_status st = validate(p);
   if (st != SV_OK) return st;
@@ -962,10 +972,11 @@ sv_status make_plan(const sv_attn_params* p, Plan* plan) {
   const int tiles = (pages + kPagesPerTile - 1) / kPagesPerTile + 1;
   const bool force_paired = (p->flags & SV_ATTN_KERNEL_PAIRED) != 0;
   const bool force_wide = (p->flags & SV_ATTN_KERNEL_WIDE) != 0;
+  const bool force_dealt = (p->flags & SV_ATTN_KERNEL_DEALT) != 0;
   // With an explicit split count the workspace does not depend on the
   // device, so host-only queries fall back to GB300's figures.
   int sms = 152, pairs = 76;
-  if (p->num_splits == 0 || (!force_paired && !force_wide)) {
+  if (p->num_splits == 0 || (!force_paired && !force_wide) || force_dealt) {
     const int n = device_sm_count();
     if (n > 0) {
       sms = n;
@@ -981,10 +992,26 @@ sv_status make_plan(const sv_attn_params* p, Plan* plan) {
   double cost_p = 0, cost_w = 0;
   const int sp = best_splits(kp, tiles, p->num_splits, &cost_p);
   const int sw = best_splits(kw, tiles, p->num_splits, &cost_w);
-  plan->wide = force_wide ? 1 : force_paired ? 0 : (cost_w < cost_p ? 1 : 0);
-  plan->splits = plan->wide ? sw : sp;
-  plan->mode = plan->splits > 1 ? kReduceGlobal : kReduceNone;
+  // The dealt kernel: one CTA per SM shares the call's weighted tiles (a
+  // 256-row tile weighs two 128-row ones) evenly; its per-tile cost is the
+  // 256-row kernel's, and its combine always runs (the host cannot tell which
+  // units the ranges cut).  The weight is bounded with the host's maxima.
+  plan->ctas = min(sms, 256);  // a merge lists at most 256 pieces (two per softmax thread)
+  const long long m_tiles = (static_cast<long long>(p->max_nodes) * plan->group + kTileRows - 1) / kTileRows;
+  const long long w_est = static_cast<long long>(p->batch) * p->num_kv_heads * tiles * m_tiles;
+  const double cost_d = kw.fixed + 0.5 * kw.per_tile * static_cast<double>((w_est + sms - 1) / sms) + 5.0;
+  // The dealt kernel is chosen only when forced: measured on GB300 its unit
+  // switches cost more than the second wave they remove (serving mix 104 vs
+  // 69 us for the 256-row kernel), so the model keeps the split kernels.
+  (void)cost_d;
+  if (force_dealt) plan->wide = 2;
+  else if (force_wide) plan->wide = 1;
+  else if (force_paired) plan->wide = 0;
+  else plan->wide = cost_w < cost_p ? 1 : 0;
+  plan->splits = plan->wide == 1 ? sw : plan->wide == 0 ? sp : 1;
+  plan->mode = (plan->wide != 2 && plan->splits > 1) ? kReduceGlobal : kReduceNone;
   size_t ws = kWorkspaceHeader;
+  if (plan->wide == 2) ws += dealt_workspace_bytes(plan->ctas, p->head_dim, dealt_units(p, plan->group));
   if (plan->mode != kReduceNone) {
     const size_t rows = static_cast<size_t>(p->total_nodes) * p->num_q_heads;
     ws += align_up(static_cast<size_t>(plan->splits) * rows * p->head_dim * 2, 256);  // bf16 O / l
@@ -1062,6 +1089,15 @@ sv_status launch(const sv_attn_params* p, const Plan& plan, cudaStream_t stream)
   const float scale = (p->sm_scale > 0.f) ? p->sm_scale : 1.0f / sqrtf(static_cast<float>(D));
   kp.scale_log2 = scale * 1.4426950408889634f;
 
+  if (plan.wide == 2) {
+    const size_t prow = static_cast<size_t>(plan.ctas) * 2 * 256;
+    uint8_t* part = ws + kWorkspaceHeader;
+    uint8_t* plse = part + align_up(prow * D * 2, 256);
+    uint8_t* cnt = plse + align_up(prow * sizeof(float), 256);
+    const DealtLaunch dl{plan.ctas, part, reinterpret_cast<float*>(plse), reinterpret_cast<int*>(cnt), kp.err,
+                         kp.trace, kp.trace_ctas};
+    return launch_dealt_attention(p, dl, stream);
+  }
   if (plan.wide) {
     const WideLaunch w{plan.splits, kp.part_o, kp.part_lse, kp.err, kp.trace, kp.trace_ctas};
     const sv_status ws = launch_wide_attention(p, w, stream);

@@ -106,7 +106,9 @@ def tree_chain(n: int) -> np.ndarray:
 
 def tree_random_depth(rng: np.random.Generator, n: int, depth: int) -> np.ndarray:
     """parent[i] uniform over earlier nodes of depth < ``depth``; redrawn until
-    the tree reaches exactly that depth."""
+    the tree reaches exactly that depth (at most n - 1)."""
+    if not 0 <= depth <= n - 1:
+        raise ValueError(f"a tree of {n} nodes cannot have depth {depth}")
     while True:
         par = [-1]
         dep = [0]

@@ -73,8 +73,10 @@ def _fake_params(**over):
     (dict(kv_pages=1 << 20), 1),                     # list without prefix sums
     (dict(batch=0), 1),
     (dict(split_reduce=1), 1),                       # only 0 (auto) and 2 (partials) exist
-    (dict(flags=8), 1),                              # unknown option bit
-    (dict(flags=6), 1),                              # both kernels forced
+    (dict(flags=16), 1),                             # unknown option bit
+    (dict(flags=6), 1),                              # two kernels forced
+    (dict(flags=10), 1),
+    (dict(flags=12), 1),
 ])
 def test_attention_host_validation(lib, over, status):
     p = _fake_params(**over)
@@ -90,6 +92,15 @@ def test_attention_workspace_size_with_explicit_splits(lib):
     assert binding.sv_tree_attention_workspace_size(p2) >= 256 + 4 * rows * 128 * 2 + 4 * rows * 4
     p1 = _fake_params(num_splits=1)
     assert binding.sv_tree_attention_workspace_size(p1) == 256
+
+
+def test_attention_workspace_size_of_the_dealt_kernel(lib):
+    # one CTA per SM (152 on GB300 when no device answers), two partial
+    # pieces of 256 rows each: bf16 O / l and fp32 log2-sum-exp; a counter
+    # per (sequence, KV head, 256-row group) and M tile, padded to 256 bytes
+    p = _fake_params(num_splits=4, flags=binding.SV_ATTN_KERNEL_DEALT)
+    rows = 152 * 2 * 256
+    assert binding.sv_tree_attention_workspace_size(p) == 256 + rows * 128 * 2 + rows * 4 + 256
 
 
 def test_attention_null_params(lib):
@@ -211,6 +222,17 @@ def test_partial_list_extend_host_validation(lib):
     assert f(a, a, a, a, 0, a, a, None, 0, None) == 1         # empty batch
     assert f(a, a, a, a, 2, None, a, None, 0, None) == 1      # no output list
     assert f(a, a, a, a, 2, a, a, a, 16, None) == 4           # workspace below its header
+
+
+def test_specpv_full_trees_host_validation(lib):
+    a = 1 << 20
+    f = lib.sv_specpv_full_trees
+    assert f(None, a, a, a, a, 2, a, a, a, None, 0, None) == 1   # no candidate parents
+    assert f(a, a, a, a, None, 2, a, a, a, None, 0, None) == 1   # no buffer offsets
+    assert f(a, a, a, a, a, 0, a, a, a, None, 0, None) == 1      # empty batch
+    assert f(a, a, a, a, a, 2, a, a, None, None, 0, None) == 1   # no output offsets
+    assert f(a, a, a, a, a, 2, a, a, a, a, 16, None) == 4        # workspace below its header
+    assert f(a, a, a, a, a, 70000, a, a, a, None, 0, None) == 2  # batch beyond one grid dimension
 
 
 def test_specpv_schedule_matches_the_oracle(lib):

@@ -56,7 +56,7 @@ def _check(case, partial=False, num_splits=0, seqs=None, kv_heads=None, sm_scale
 
 
 # the library's choice, then each kernel forced
-KERNELS = [0, binding.SV_ATTN_KERNEL_PAIRED, binding.SV_ATTN_KERNEL_WIDE]
+KERNELS = [0, binding.SV_ATTN_KERNEL_PAIRED, binding.SV_ATTN_KERNEL_WIDE, binding.SV_ATTN_KERNEL_DEALT]
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
@@ -260,3 +260,53 @@ def test_pair_with_an_empty_row_tile(nodes, splits, kernel):
                      with_logits=False, seed=nodes + 11)
     for _ in range(2):
         _check(case, num_splits=splits, split_reduce=2 if splits > 1 else 0, flags=kernel)
+
+
+@pytest.mark.parametrize("ctx", [[0], [17], [0, 0, 129], [5000]])
+def test_dealt_ranges_narrower_than_a_tile(ctx):
+    # a call whose total weight is below (or near) twice the CTA count: most
+    # CTAs hold no tile or one 256-row tile (weight 2), some ranges fall
+    # between two tile starts, and the combine must skip those CTAs
+    case = make_case("llama8b_eagle", layers=1, batch=len(ctx), ctx=ctx, with_logits=False, seed=len(ctx) + 3)
+    _check(case, flags=binding.SV_ATTN_KERNEL_DEALT)
+
+
+def test_dealt_plan_reports_its_kernel():
+    case = make_case("serving_mix", with_logits=False)
+    dc = DeviceCase(case, layers=[0])
+    c = case
+    out = torch.empty((c.total_nodes, c.num_q_heads, c.head_dim), dtype=torch.bfloat16, device="cuda")
+    p = binding.make_attn_params(q=dc.q[0], tree_k=dc.tree_k[0], tree_v=dc.tree_v[0], k_cache=dc.k_cache[0],
+                                 v_cache=dc.v_cache[0], block_table=dc.block_table, ctx_lens=dc.ctx_lens,
+                                 cu_nodes=dc.cu_nodes, parents=dc.parents, out=out, total_nodes=c.total_nodes,
+                                 max_nodes=c.max_nodes, flags=binding.SV_ATTN_KERNEL_DEALT)
+    splits, reduce, kernel = binding.sv_tree_attention_plan(p, with_kernel=True)
+    assert (splits, reduce, kernel) == (1, 0, 2)
+
+
+def test_dealt_workspace_left_ready_for_the_next_call():
+    # cut units are merged by their last piece, which resets the unit's
+    # counter: two calls on one workspace give the oracle's answer, and the
+    # counters (the workspace's tail) are zero after each
+    case = make_case("serving_mix", batch=5, ctx=(300, 2500), with_logits=False, seed=41)
+    dc = DeviceCase(case, layers=[0])
+    c = case
+    ref, ref_lse = _oracle(case)
+    out = torch.empty((c.total_nodes, c.num_q_heads, c.head_dim), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((c.total_nodes, c.num_q_heads), dtype=torch.float32, device="cuda")
+    p = binding.make_attn_params(q=dc.q[0], tree_k=dc.tree_k[0], tree_v=dc.tree_v[0], k_cache=dc.k_cache[0],
+                                 v_cache=dc.v_cache[0], block_table=dc.block_table, ctx_lens=dc.ctx_lens,
+                                 cu_nodes=dc.cu_nodes, parents=dc.parents, out=out, lse=lse,
+                                 total_nodes=c.total_nodes, max_nodes=c.max_nodes, flags=binding.SV_ATTN_KERNEL_DEALT)
+    n = binding.sv_tree_attention_workspace_size(p)
+    ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    p.workspace, p.workspace_bytes = ws.data_ptr(), n
+    units = c.batch * c.num_kv_heads * ((c.max_nodes * (c.num_q_heads // c.num_kv_heads) + 255) // 256)
+    for _ in range(2):
+        out.fill_(float("nan"))
+        binding.sv_tree_attention(p)
+        torch.cuda.synchronize()
+        assert binding.sv_get_device_error(ws) == 0
+        _compare(case, out.float().cpu().numpy(), lse.cpu().numpy(), ref, ref_lse)
+        tail = ws[n - ((units * 8 + 255) // 256) * 256:]
+        assert int(tail.count_nonzero()) == 0
