@@ -318,6 +318,10 @@ sv_status sv_sample_accept(const float* logits, const float* draft_probs, int vo
  * which commits nothing for b and records SV_DEVERR_DEPTH); it must not
  * alias ctx_lens.  The caller
  * guarantees pages for slots L_b .. L_b + max_depth.  Nothing else changes.
+ * The kernel is launched as a programmatic dependent of whatever kernel
+ * precedes it on the stream (sv_greedy_accept and sv_sample_accept let it
+ * start at once): it waits for that kernel's completion before reading
+ * accept_len and accepted_nodes, so the ordering is the stream's as usual.
  *
  * tree_k/tree_v: bf16 [num_layers][T, Hkv, D], layer stride
  * tree_layer_stride elements.  k_cache/v_cache: bf16

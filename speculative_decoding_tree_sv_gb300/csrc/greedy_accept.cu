@@ -203,6 +203,9 @@ __device__ void walk_sequence(const Params& p, int b, int n0, int N, uint8_t* sc
 
 __global__ void __launch_bounds__(kThreads) greedy_accept_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) uint8_t dyn[];  // [kSmemPart] floats, then the walk's arrays
+  // A following KV commit (launched as a programmatic dependent) may become
+  // resident now; it waits for this grid to complete before reading the path.
+  griddep_launch_dependents();
   __shared__ int s_b, s_n0, s_n, s_last;
   __shared__ float s_v[kThreads / 32];
   __shared__ int s_i[kThreads / 32];

@@ -8,6 +8,9 @@
 // KV heads: a bit copy in 16-byte vectors.  One CTA per (j, b, layer); CTAs
 // with j > accept_len[b] exit at once.  Source (dense tree buffer) and
 // destination (paged cache) never overlap, so the copy needs no ordering.
+// The launch is a programmatic dependent of the preceding kernel (the
+// acceptance, which lets it become resident at once): no launch gap between
+// them, and every CTA waits for that kernel's results before reading them.
 #include "sv_device.cuh"
 
 namespace sv {
@@ -39,6 +42,9 @@ __global__ void __launch_bounds__(256) kv_commit_kernel(const __grid_constant__ 
   const int j = blockIdx.x;
   const int b = blockIdx.y;
   const int layer = blockIdx.z;
+  // Launched as a programmatic dependent of the acceptance: the CTAs are
+  // resident while it runs and read the accepted path once it has completed.
+  griddep_wait();
   const int a = p.accept_len[b];
   if (j > a) return;
   const int L = p.ctx_lens[b];
@@ -135,8 +141,15 @@ extern "C" sv_status sv_kv_commit(const void* tree_k, const void* tree_v, long l
   p.page_size = page_size;
   const int per = 2 * num_kv_heads * (head_dim / 8);
   const int threads = per >= 256 ? 256 : ((per + 31) / 32) * 32;
-  dim3 grid(max_depth + 1, batch, num_layers);
-  commit::kv_commit_kernel<<<grid, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+  cudaLaunchConfig_t cfg = cudaLaunchConfig_t{};
+  cfg.gridDim = dim3(max_depth + 1, batch, num_layers);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, commit::kv_commit_kernel, p) != cudaSuccess) return SV_ERR_CUDA;
   return SV_OK;
 }

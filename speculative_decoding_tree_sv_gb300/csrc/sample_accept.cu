@@ -300,6 +300,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
 
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kWalkThreads)
     walk_kernel(const __grid_constant__ WalkParams p) {
+  // a following KV commit may become resident now (it waits for completion)
+  griddep_launch_dependents();
   __shared__ float slots[3];  // this CTA's residual total, found token, last token with mass
   __shared__ float s_mz[1 + kMaxZ];
   __shared__ float s_inv[kMaxZ];
