@@ -558,7 +558,7 @@ class AttentionLeg:
     `replicas` times (distinct addresses) so the calls of one replay read
     more than twice the L2 from HBM."""
 
-    def __init__(self, torch, case, partial, dev, bytes_per_call, flags: int = 0):
+    def __init__(self, torch, case, partial, dev, bytes_per_call, flags: int = 0, num_splits: int = 0):
         from speculative_decoding_tree_sv_gb300 import binding
         self.torch, self.binding, self.case, self.partial = torch, binding, case, partial
         c = case
@@ -596,7 +596,7 @@ class AttentionLeg:
                 v_cache=self.v_cache[r], block_table=self.block_table, ctx_lens=self.ctx_lens,
                 cu_nodes=self.cu_nodes, parents=self.parents, out=self.out[r], total_nodes=c.total_nodes,
                 max_nodes=c.max_nodes, kv_pages=self.kv_pages, cu_kv_pages=self.cu_kv_pages,
-                max_kv_pages=max_kv, flags=flags)
+                max_kv_pages=max_kv, flags=flags, num_splits=num_splits)
             ws_bytes = max(ws_bytes, binding.sv_tree_attention_workspace_size(p))
             self.params.append(p)
         self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)

@@ -115,10 +115,10 @@ enum sv_attn_flags {
    * by cluster multicast, scores double-buffered in TMEM; suits short
    * contexts split across many CTAs.  WIDE: one CTA per 256-row group, each
    * K/V tile staged in one SM only, the context split evenly per group.
-   * DEALT: the WIDE engine in one CTA per SM, the call's whole work (every
-   * sequence, KV head and row group, weighted by 128-row tiles) dealt to
-   * the CTAs in equal contiguous ranges, so batches of uneven or many
-   * sequences run in one even wave; suits long and batched contexts. */
+   * DEALT: the WIDE engine in one CTA per SM (a multiple of Hkv), groups of
+   * one CTA per KV head taking equal contiguous ranges of the call's
+   * (sequence, row group, tile) work, so batches of uneven or many
+   * sequences run in one even wave. */
   SV_ATTN_KERNEL_PAIRED = 2,
   SV_ATTN_KERNEL_WIDE = 4,
   SV_ATTN_KERNEL_DEALT = 8

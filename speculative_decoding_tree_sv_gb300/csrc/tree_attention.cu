@@ -992,14 +992,16 @@ sv_status make_plan(const sv_attn_params* p, Plan* plan) {
   double cost_p = 0, cost_w = 0;
   const int sp = best_splits(kp, tiles, p->num_splits, &cost_p);
   const int sw = best_splits(kw, tiles, p->num_splits, &cost_w);
-  // The dealt kernel: one CTA per SM shares the call's weighted tiles (a
-  // 256-row tile weighs two 128-row ones) evenly; its per-tile cost is the
-  // 256-row kernel's, and its combine always runs (the host cannot tell which
-  // units the ranges cut).  The weight is bounded with the host's maxima.
-  plan->ctas = min(sms, 256);  // a merge lists at most 256 pieces (two per softmax thread)
+  // The dealt kernel: one CTA per SM shares the call's tiles evenly; its
+  // per-tile cost is the 256-row kernel's, plus merges of the units its
+  // ranges cut.  The tile count is bounded with the host's maxima.
+  // a multiple of Hkv (groups of one CTA per KV head), at most 256 (a merge
+  // lists at most two pieces per softmax thread)
+  plan->ctas = (min(sms, 256) / p->num_kv_heads) * p->num_kv_heads;
+  if (force_dealt && plan->ctas < p->num_kv_heads) return SV_ERR_UNSUPPORTED;
   const long long m_tiles = (static_cast<long long>(p->max_nodes) * plan->group + kTileRows - 1) / kTileRows;
-  const long long w_est = static_cast<long long>(p->batch) * p->num_kv_heads * tiles * m_tiles;
-  const double cost_d = kw.fixed + 0.5 * kw.per_tile * static_cast<double>((w_est + sms - 1) / sms) + 5.0;
+  const long long w_est = static_cast<long long>(p->batch) * p->num_kv_heads * tiles * ((m_tiles + 1) / 2);
+  const double cost_d = kw.fixed + kw.per_tile * static_cast<double>((w_est + sms - 1) / sms) + 5.0;
   // The dealt kernel is chosen only when forced: measured on GB300 its unit
   // switches cost more than the second wave they remove (serving mix 104 vs
   // 69 us for the 256-row kernel), so the model keeps the split kernels.

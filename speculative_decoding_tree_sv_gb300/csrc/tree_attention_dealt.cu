@@ -7,12 +7,13 @@
 // call's work evenly, whatever the batch's lengths.
 //
 //   * A unit is (sequence, KV head, 256-row group); its work is its context
-//     tiles (128 keys each) plus the tree tile, each weighted by the unit's
-//     128-row M tiles (1 or 2).  Units are laid end to end in (sequence, KV
-//     head, group) order; CTA c takes the tiles whose weighted start lies in
-//     [c W / C, (c + 1) W / C), W being the call's total weight.  So every CTA
-//     does the same work up to one tile: no second wave (a batch whose units
-//     outnumber the SMs) and no idle SMs (long sequences next to short ones).
+//     tiles (128 keys each) plus the tree tile.  The CTAs form groups of Hkv,
+//     one CTA per KV head: the (sequence, row group, tile) list of one head
+//     is cut into equal contiguous ranges, one per group, and CTA kh of a
+//     group does that range for KV head kh.  So every CTA streams the same
+//     number of tiles up to one (no second wave when units outnumber the
+//     SMs, no idle SMs beside long sequences), and the Hkv CTAs of a group
+//     read the same pages' head slices at about the same time.
 //   * A CTA walks its range unit by unit ("pieces"): the K/V ring, the MMA
 //     order and every barrier phase run on across pieces, so the next piece's
 //     tiles load while the previous one drains.  Q of the next piece is
@@ -48,6 +49,13 @@ constexpr int kTileRows = 128;  // rows per M tile
 constexpr int kGroupRows = 256;  // two M tiles per unit
 constexpr int kPagesPerTile = kBlockN / 16;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: defer O rescale until max grows by 2^8
+// The scheduler warp lists a CTA's pieces after its first in shared memory
+// (the first comes straight from the range's start); a range with more
+// continues with a cursor from where the list ends.
+constexpr int kMaxListed = 40;
+constexpr int kPieceBytes = 96;
+constexpr int kCursorBytes = 112;
+constexpr uint32_t kListBytes = kMaxListed * kPieceBytes + kCursorBytes + 16;
 constexpr float kLn2 = 0.69314718055994530942f;
 
 template <int D>
@@ -72,7 +80,9 @@ struct Cfg {
   // passes of eight)
   static constexpr uint32_t kStageRows = 8;
   static constexpr uint32_t kStageWarpBytes = kStageRows * D * 2;
-  static constexpr uint32_t kSmemBytes = kOffStage + 8 * kStageWarpBytes + 1024;  // + alignment slack
+  // the CTA's pieces after its first, written by the scheduler warp
+  static constexpr uint32_t kOffList2 = kOffStage + 8 * kStageWarpBytes;
+  static constexpr uint32_t kSmemBytes = kOffList2 + kListBytes + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128;
   static constexpr uint32_t kColO0 = 256, kColO1 = 256 + D;
@@ -109,7 +119,7 @@ struct Params {
 // than max_nodes has no work (it is reported once, by CTA 0).
 struct Seq {
   int n0, N, L, n_pages, kvp0, last_page_tokens, t_ctx, t_all, mtiles, groups;
-  long long weight;  // Hkv * t_all * mtiles
+  long long weight;  // tiles of one KV head: t_all * groups
 };
 
 __device__ __forceinline__ Seq seq_info(const Params& p, int b) {
@@ -136,19 +146,19 @@ __device__ __forceinline__ Seq seq_info(const Params& p, int b) {
   const int rows = valid ? s.N * p.group : 0;
   s.mtiles = (rows + kTileRows - 1) / kTileRows;
   s.groups = (rows + kGroupRows - 1) / kGroupRows;
-  s.weight = static_cast<long long>(p.num_kv_heads) * s.t_all * s.mtiles;
+  s.weight = static_cast<long long>(s.t_all) * s.groups;
   return s;
 }
 
 __device__ __forceinline__ long long llmin(long long a, long long b) { return a < b ? a : b; }
 
-// Range of CTA c: weighted positions [lo, hi) of W.
+// Range of CTA group g of C groups: tile positions [lo, hi) of W.
 __device__ __forceinline__ long long range_start(long long W, int c, int C) {
   return W * c / C;
 }
 
-// The CTA whose range holds weighted position pos.
-__device__ __forceinline__ int cta_of(long long W, long long pos, int C) {
+// The group whose range holds tile position pos.
+__device__ __forceinline__ int group_of(long long W, long long pos, int C) {
   return static_cast<int>(((pos + 1) * C - 1) / W);
 }
 
@@ -158,15 +168,16 @@ struct Piece {
   int ja, je;             // tiles [ja, je) of the unit's t_all
   int nt;                 // M tiles of the unit (1 or 2)
   int slot;               // -1: whole unit (writes the output); 0 / 1: partial slot
-  long long pos;          // the unit's weighted start
+  long long pos;          // the unit's first tile in its head's list
   Seq s;
 };
 
-// Walks the units that intersect [lo, hi) in order.  Every role of a CTA
-// runs its own cursor over the same pieces.  Start: the first unit of the
-// range (b, kh, mg) and its weighted start pos, as found by locate().
+// Walks the units of one KV head that intersect [lo, hi) in order.  Every
+// role of a CTA runs its own cursor over the same pieces.  Start: the first
+// unit of the range (b, mg) and its first tile's position pos, as found by
+// locate().
 struct Cursor {
-  long long lo, hi, pos;  // range, weighted start of the current unit
+  long long lo, hi, pos;  // range, position of the current unit's first tile
   int b, kh, mg;
   Seq s;
   bool have;              // s describes sequence b
@@ -186,16 +197,13 @@ __device__ bool next_piece(const Params& p, Cursor& c, Piece& out) {
     }
     if (c.s.weight == 0 || c.mg >= c.s.groups) {  // next sequence
       ++c.b;
-      c.kh = 0;
       c.mg = 0;
       c.have = false;
       continue;
     }
-    const int nt = unit_mtiles(c.s, c.mg);
-    const long long w = static_cast<long long>(c.s.t_all) * nt;
-    // tiles whose weighted start lies in [lo, hi) (nt is 1 or 2)
-    const long long a = c.lo > c.pos ? ((c.lo - c.pos + nt - 1) >> (nt - 1)) : 0;
-    const long long e = (c.hi - c.pos + nt - 1) >> (nt - 1);
+    // tiles whose position lies in [lo, hi)
+    const long long a = c.lo > c.pos ? c.lo - c.pos : 0;
+    const long long e = c.hi - c.pos;
     const int ja = static_cast<int>(llmin(a, c.s.t_all));
     const int je = static_cast<int>(llmin(e, c.s.t_all));
     out.b = c.b;
@@ -203,32 +211,45 @@ __device__ bool next_piece(const Params& p, Cursor& c, Piece& out) {
     out.mg = c.mg;
     out.ja = ja;
     out.je = je;
-    out.nt = nt;
+    out.nt = unit_mtiles(c.s, c.mg);
     out.s = c.s;
     const bool whole = ja == 0 && je == c.s.t_all;
     out.slot = whole ? -1 : (c.pos <= c.lo ? 0 : 1);
     out.pos = c.pos;
     // advance to the next unit
-    c.pos += w;
+    c.pos += c.s.t_all;
     if (++c.mg >= c.s.groups) {
       c.mg = 0;
-      if (++c.kh >= p.num_kv_heads) {
-        c.kh = 0;
-        ++c.b;
-        c.have = false;
-      }
+      ++c.b;
+      c.have = false;
     }
     if (ja < je) return true;
   }
 }
 
-// The unit holding weighted position lo (first unit whose end is past lo),
-// by one warp: per-sequence weights are summed in chunks of 32 with a warp
-// prefix scan.  Also returns the total weight W.  CTA 0 reports trees with
-// no node or more than max_nodes.
-__device__ void locate(const Params& p, int C, int cta, long long* W_out, Cursor* cur) {
+// Piece k of this CTA for a role: the first from the role's own cursor, the
+// next ones from the scheduler warp's list (the caller has waited for it
+// before asking for piece 1), beyond the list from a cursor where the list
+// ended.  False when the range is done.
+__device__ bool get_piece(const Params& p, int k, Cursor& cur, Piece& pc, const Piece* list, const int* nlist,
+                          const Cursor* cont) {
+  if (k == 0) return next_piece(p, cur, pc);
+  const int n = *nlist;
+  if (k - 1 < n) {
+    pc = list[k - 1];
+    return true;
+  }
+  if (n < kMaxListed) return false;  // the list held every remaining piece
+  if (k - 1 == n) cur = *cont;
+  return next_piece(p, cur, pc);
+}
+
+// The unit holding position lo of group g's range (the first unit whose end
+// is past lo), by one warp: per-sequence tile counts are summed in chunks of
+// 32 with a warp prefix scan.  Also returns the total W.  CTA 0 reports trees
+// with no node or more than max_nodes.
+__device__ void locate(const Params& p, int ngroups, int g, int kh, int cta, long long* W_out, Cursor* cur) {
   const int lane = threadIdx.x & 31;
-  // total weight
   long long tot = 0;
   for (int b0 = 0; b0 < p.batch; b0 += 32) {
     const int b = b0 + lane;
@@ -244,9 +265,10 @@ __device__ void locate(const Params& p, int C, int cta, long long* W_out, Cursor
   }
   const long long W = tot;
   *W_out = W;
-  cur->lo = W > 0 ? range_start(W, cta, C) : 0;
-  cur->hi = W > 0 ? range_start(W, cta + 1, C) : 0;
+  cur->lo = W > 0 ? range_start(W, g, ngroups) : 0;
+  cur->hi = W > 0 ? range_start(W, g + 1, ngroups) : 0;
   cur->have = false;
+  cur->kh = kh;
   // sequence holding lo
   long long base = 0;
   int bsel = p.batch;
@@ -269,21 +291,14 @@ __device__ void locate(const Params& p, int C, int cta, long long* W_out, Cursor
     }
   }
   cur->b = bsel;
-  cur->kh = 0;
   cur->mg = 0;
   cur->pos = base;
   if (bsel < p.batch) {
-    // inside sequence b: KV heads of weight t_all * mtiles each, then groups
-    // of weight 2 * t_all (the last group may have one M tile)
+    // inside sequence b: row groups of t_all tiles each
     const Seq s = seq_info(p, bsel);
-    const long long per_head = static_cast<long long>(s.t_all) * s.mtiles;
-    const long long off = cur->lo - base;
-    const int kh = static_cast<int>(llmin(off / per_head, p.num_kv_heads - 1));
-    const long long hoff = off - kh * per_head;
-    const int mg = static_cast<int>(llmin(hoff / (2LL * s.t_all), s.groups - 1));
-    cur->kh = kh;
+    const int mg = static_cast<int>(llmin((cur->lo - base) / s.t_all, s.groups - 1));
     cur->mg = mg;
-    cur->pos = base + kh * per_head + 2LL * s.t_all * mg;
+    cur->pos = base + static_cast<long long>(s.t_all) * mg;
     cur->s = s;
     cur->have = true;
   }
@@ -302,7 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int G = p.group;
   const int cta = blockIdx.x;
-  const int ncta = gridDim.x;
+  const int ngroups = gridDim.x / p.num_kv_heads;  // the grid is a multiple of Hkv
+  const int grp = cta / p.num_kv_heads;
+  const int kh_cta = cta - grp * p.num_kv_heads;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* q_full = bars;
@@ -315,7 +332,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_full + 2;     // [2]
   uint64_t* o_final = p_full + 2;    // [2]
   uint64_t* drain = o_final + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* list_ready = drain + 1;  // the scheduler warp has written the piece list
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(list_ready + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* never_set = abort_flag + 1;
   int* par_s = reinterpret_cast<int*>(smem + C::kOffPar);
@@ -324,6 +342,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* flag_s = wcount_s + 8;                                       // [2]
   long long* W_s = reinterpret_cast<long long*>(smem + C::kOffCount + 48);
   Cursor* start = reinterpret_cast<Cursor*>(smem + C::kOffBar + 256);
+  Piece* list = reinterpret_cast<Piece*>(smem + C::kOffList2);
+  Cursor* cont = reinterpret_cast<Cursor*>(smem + C::kOffList2 + kMaxListed * kPieceBytes);
+  int* nlist = reinterpret_cast<int*>(smem + C::kOffList2 + kMaxListed * kPieceBytes + kCursorBytes);
+  static_assert(sizeof(Piece) <= kPieceBytes && sizeof(Cursor) <= kCursorBytes, "piece list layout");
   static_assert(256 + sizeof(Cursor) <= C::kBarBytes - 8, "schedule fits beside the barriers");
   // phase tracing (diagnostics): no live registers when it is off
   long long* trace_clk0 = reinterpret_cast<long long*>(smem + C::kOffBar + C::kBarBytes - 8);
@@ -352,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(o_final + t, 1);
     }
     mbar_init(drain, 1);
+    mbar_init(list_ready, 1);
     *abort_flag = 0;
     *never_set = 0;
     fence_mbar_init();
@@ -370,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 2) {
     long long W;
     Cursor cur;
-    locate(p, ncta, cta, &W, &cur);
+    locate(p, ngroups, grp, kh_cta, cta, &W, &cur);
     if (lane == 0) {
       *start = cur;
       *W_s = W;
@@ -393,7 +416,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int k_issued = 0, v_issued = 0;
       int q_issued = 0;   // pieces whose Q was requested
       bool ok = true;
-      for (int k = 0; ok && next_piece(p, cur, pc); ++k) {
+      for (int k = 0; ok; ++k) {
+        if (k == 1) {
+          int w = (lane == 0) ? (mbar_wait(list_ready, 0, abort_flag) ? 1 : 0) : 0;
+          if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+        }
+        if (!get_piece(p, k, cur, pc, list, nlist, cont)) break;
         const Seq& s = pc.s;
         const int row0 = pc.mg * kGroupRows;
         for (int j = pc.ja; j < pc.je; ++j, ++g) {
@@ -477,6 +505,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = max(0, v_issued - NST); i < v_issued; ++i)
           mbar_wait(v_full + (i % NST), (i / NST) & 1, never_set);
       }
+    } else if (warp == 2) {
+      // ------------------------------------------------------------ scheduler
+      // Lists the CTA's pieces after the first while the first one runs, so
+      // the other roles find the next unit's facts in shared memory.
+      if (lane == 0) {
+        Cursor c = cur0;
+        Piece tmp;
+        int n = 0;
+        if (next_piece(p, c, tmp)) {  // the first piece: every role derives it itself
+          while (n < kMaxListed && next_piece(p, c, tmp)) list[n++] = tmp;
+        }
+        *cont = c;
+        *nlist = n;
+        mbar_arrive(list_ready);
+      }
+      __syncwarp();
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
       if (lane == 0) {
@@ -509,7 +553,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int g = 0;                // ring position of the piece's first tile
         int tiles_t[2] = {0, 0};  // tiles handed to each M tile's softmax before this piece
-        for (int k = 0; ok && next_piece(p, cur, pc); ++k) {
+        for (int k = 0; ok; ++k) {
+          if (k == 1 && !mbar_wait(list_ready, 0, abort_flag)) { ok = false; break; }
+          if (!get_piece(p, k, cur, pc, list, nlist, cont)) break;
           const int nt = pc.nt;
           const int n = pc.je - pc.ja;
           const int st0 = g % NST;
@@ -581,7 +627,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     Cursor cur = cur0;
     Piece pc;
-    while (ok && next_piece(p, cur, pc)) {
+    Piece cut[2];  // this CTA's pieces of cut units (its first and its last), merged at the end
+    int ncut = 0;
+    for (int k = 0; ok; ++k) {
+      if (k == 1 && !__all_sync(0xffffffffu, mbar_wait(list_ready, 0, abort_flag))) { ok = false; break; }
+      if (!get_piece(p, k, cur, pc, list, nlist, cont)) break;
       if (t >= pc.nt) continue;  // this M tile has no rows in the unit
       const Seq& s = pc.s;
       const int row = pc.mg * kGroupRows + t * kTileRows + r;
@@ -775,98 +825,149 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.part_lse[(static_cast<size_t>(cta) * 2 + pc.slot) * kGroupRows + prow] = lse2;
         }
       }
-      if (pc.slot >= 0) {
-        // ------------------------------------------------ merge of a cut unit
-        // The unit's pieces are in the CTAs first..last that hold its tiles
-        // (a range narrower than one tile's weight may hold none).  Each piece
-        // counts itself once its partial rows are written; the last to count
-        // merges them all (no waiting on another CTA) and leaves the counter
-        // at zero for the next call.
-        const long long W = *W_s;
-        const int ncta = gridDim.x;
-        const int first = cta_of(W, pc.pos, ncta);
-        const int last = cta_of(W, pc.pos + static_cast<long long>(s.t_all - 1) * pc.nt, ncta);
-        const int span = last - first + 1;  // <= 256 (one CTA per SM)
-        // the list of pieces, in CTA order: per warp of the group a ballot,
-        // the warps' counts in shared memory, then each warp's base
-        int total = 0;
-        for (int i0 = 0; i0 < span; i0 += kTileRows) {
-          const int i = i0 + r;
-          bool holds = false;
-          int base_row = 0;
-          if (i < span) {
-            const int c = first + i;
-            const long long lo = range_start(W, c, ncta), hi = range_start(W, c + 1, ncta);
-            const long long ja = lo > pc.pos ? ((lo - pc.pos + pc.nt - 1) >> (pc.nt - 1)) : 0;
-            holds = ja < s.t_all && pc.pos + ja * pc.nt < hi;
-            base_row = (c * 2 + (pc.pos <= lo ? 0 : 1)) * kGroupRows;
-          }
-          const unsigned bal = __ballot_sync(0xffffffffu, holds);
-          if (lane == 0) wcount_s[t * 4 + qw] = __popc(bal);
-          named_barrier(4 + t, kTileRows);
-          int base = total;
-          for (int w = 0; w < qw; ++w) base += wcount_s[t * 4 + w];
-          if (holds) list_t[base + __popc(bal & ((1u << lane) - 1u))] = base_row;
-          for (int w = 0; w < 4; ++w) total += wcount_s[t * 4 + w];
-          named_barrier(4 + t, kTileRows);
-        }
-        __threadfence();  // this piece's partial rows, before it is counted
-        named_barrier(4 + t, kTileRows);
-        const int u = (pc.b * p.num_kv_heads + pc.kh) * p.groups_max + pc.mg;
-        if (r == 0) flag_s[t] = atomicAdd(p.counters + 2 * u + t, 1) == total - 1 ? 1 : 0;
-        named_barrier(4 + t, kTileRows);
-        if (flag_s[t]) {
-          if (r == 0) p.counters[2 * u + t] = 0;
-          __threadfence();
-          if (row_exists) {
-            // online merge over the pieces: O = sum w_i O_i / sum w_i with
-            // w_i = 2^(lse_i - max); one piece's row in flight at a time
-            float acc[D];
-#pragma unroll
-            for (int e = 0; e < D; ++e) acc[e] = 0.f;
-            float mx = -INFINITY, wsum = 0.f;
-            for (int i = 0; i < total; ++i) {
-              const size_t pr = static_cast<size_t>(list_t[i]) + prow;
-              const float li = __ldcg(p.part_lse + pr);
-              const uint4* src = reinterpret_cast<const uint4*>(p.part_o + pr * D);
-              uint4 v[kChunks];
-#pragma unroll
-              for (int ch = 0; ch < kChunks; ++ch) v[ch] = __ldcg(src + ch);
-              if (li == -INFINITY) continue;
-              if (li > mx) {
-                const float f = (mx == -INFINITY) ? 0.f : ex2(mx - li);
-                wsum *= f;
-#pragma unroll
-                for (int e = 0; e < D; ++e) acc[e] *= f;
-                mx = li;
-              }
-              const float w = ex2(li - mx);
-              wsum += w;
-#pragma unroll
-              for (int ch = 0; ch < kChunks; ++ch) {
-                const uint32_t x[4] = {v[ch].x, v[ch].y, v[ch].z, v[ch].w};
-#pragma unroll
-                for (int k2 = 0; k2 < 4; ++k2) {
-                  acc[ch * 8 + 2 * k2] += w * __uint_as_float(x[k2] << 16);
-                  acc[ch * 8 + 2 * k2 + 1] += w * __uint_as_float(x[k2] & 0xFFFF0000u);
-                }
-              }
-            }
-            const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
-            uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D);
-#pragma unroll
-            for (int ch = 0; ch < kChunks; ++ch)
-              dst[ch] = make_uint4(pack_bf16x2(acc[ch * 8 + 0] * inv, acc[ch * 8 + 1] * inv),
-                                   pack_bf16x2(acc[ch * 8 + 2] * inv, acc[ch * 8 + 3] * inv),
-                                   pack_bf16x2(acc[ch * 8 + 4] * inv, acc[ch * 8 + 5] * inv),
-                                   pack_bf16x2(acc[ch * 8 + 6] * inv, acc[ch * 8 + 7] * inv));
-            if (p.lse != nullptr) p.lse[orow] = (wsum > 0.f) ? (mx + log2f(wsum)) * kLn2 : -INFINITY;
-          }
-        }
-      }
+      if (pc.slot >= 0 && ncut < 2) cut[ncut++] = pc;
       tiles_done += n;
       ++pieces_done;
       if (t == 0 && r == 0) mark(SV_TRACE_EPILOGUE);
+    }
+    // ---------------------------------------------------- merges of cut units
+    // A cut unit's pieces are in the groups first..last whose ranges hold its
+    // tiles (an empty range holds none), at the CTA of the unit's KV head.  Each piece
+    // counts itself once this CTA is done with its pieces; the last to count
+    // merges them all (no waiting on another CTA) and leaves the counter at
+    // zero for the next call.  Counting at the end keeps the count's round
+    // trip off the pipeline.
+    for (int ci = 0; ok && ci < ncut; ++ci) {
+      const Piece& q = cut[ci];
+      const Seq& s = q.s;
+      const int row = q.mg * kGroupRows + t * kTileRows + r;
+      const bool row_exists = row < s.N * G;
+      const int node = row / G;
+      const int gq = row - node * G;
+      const size_t orow = static_cast<size_t>(s.n0 + node) * p.num_q_heads + q.kh * G + gq;
+      const int prow = t * kTileRows + r;
+      const long long W = *W_s;
+      const int first = group_of(W, q.pos, ngroups);  // groups holding the unit's first and last tiles
+      const int last = group_of(W, q.pos + s.t_all - 1, ngroups);
+      const int span = last - first + 1;  // <= 256 (one CTA per SM)
+      // the list of pieces, in CTA order: per warp of the group a ballot,
+      // the warps' counts in shared memory, then each warp's base
+      int total = 0;
+      for (int i0 = 0; i0 < span; i0 += kTileRows) {
+        const int i = i0 + r;
+        bool holds = false;
+        int base_row = 0;
+        if (i < span) {
+          const int g = first + i;
+          const long long lo = range_start(W, g, ngroups), hi = range_start(W, g + 1, ngroups);
+          const long long ja = lo > q.pos ? lo - q.pos : 0;
+          holds = ja < s.t_all && q.pos + ja < hi;
+          const int c = g * p.num_kv_heads + q.kh;  // that group's CTA for this KV head
+          base_row = (c * 2 + (q.pos <= lo ? 0 : 1)) * kGroupRows;
+        }
+        const unsigned bal = __ballot_sync(0xffffffffu, holds);
+        if (lane == 0) wcount_s[t * 4 + qw] = __popc(bal);
+        named_barrier(4 + t, kTileRows);
+        int base = total;
+        for (int w = 0; w < qw; ++w) base += wcount_s[t * 4 + w];
+        if (holds) list_t[base + __popc(bal & ((1u << lane) - 1u))] = base_row;
+        for (int w = 0; w < 4; ++w) total += wcount_s[t * 4 + w];
+        named_barrier(4 + t, kTileRows);
+      }
+      // count this piece once every thread's partial rows are visible
+      // device-wide (each fences its own writes; the barrier orders the
+      // fences before thread 0's count)
+      const int u = (q.b * p.num_kv_heads + q.kh) * p.groups_max + q.mg;
+      __threadfence();
+      named_barrier(4 + t, kTileRows);
+      if (r == 0) flag_s[t] = atomicAdd(p.counters + 2 * u + t, 1) == total - 1 ? 1 : 0;
+      named_barrier(4 + t, kTileRows);
+      if (!flag_s[t]) continue;
+      if (r == 0) p.counters[2 * u + t] = 0;
+      __threadfence();
+      if (!row_exists) continue;
+      constexpr int kChunks = D / 8;
+      uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D);
+      if (total <= 2) {
+        // the common case: both rows and both log2-sum-exps in one round trip
+        float l2[2] = {-INFINITY, -INFINITY};
+        uint4 v[2][kChunks];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          if (i < total) {
+            const size_t pr = static_cast<size_t>(list_t[i]) + prow;
+            l2[i] = __ldcg(p.part_lse + pr);
+            const uint4* src = reinterpret_cast<const uint4*>(p.part_o + pr * D);
+#pragma unroll
+            for (int ch = 0; ch < kChunks; ++ch) v[i][ch] = __ldcg(src + ch);
+          } else {
+#pragma unroll
+            for (int ch = 0; ch < kChunks; ++ch) v[i][ch] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        const float mx = fmaxf(l2[0], l2[1]);
+        const float w0 = (l2[0] == -INFINITY) ? 0.f : ex2(l2[0] - mx);
+        const float w1 = (l2[1] == -INFINITY) ? 0.f : ex2(l2[1] - mx);
+        const float ws = w0 + w1;
+        const float inv = (ws > 0.f) ? 1.f / ws : 0.f;
+        const float a0 = w0 * inv, a1 = w1 * inv;
+#pragma unroll
+        for (int ch = 0; ch < kChunks; ++ch) {
+          const uint32_t x0[4] = {v[0][ch].x, v[0][ch].y, v[0][ch].z, v[0][ch].w};
+          const uint32_t x1[4] = {v[1][ch].x, v[1][ch].y, v[1][ch].z, v[1][ch].w};
+          uint32_t o4[4];
+#pragma unroll
+          for (int k2 = 0; k2 < 4; ++k2) {
+            const float lo = a0 * __uint_as_float(x0[k2] << 16) + a1 * __uint_as_float(x1[k2] << 16);
+            const float hi = a0 * __uint_as_float(x0[k2] & 0xFFFF0000u) + a1 * __uint_as_float(x1[k2] & 0xFFFF0000u);
+            o4[k2] = pack_bf16x2(lo, hi);
+          }
+          dst[ch] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+        }
+        if (p.lse != nullptr) p.lse[orow] = (ws > 0.f) ? (mx + log2f(ws)) * kLn2 : -INFINITY;
+      } else {
+        // more pieces (a unit longer than a CTA's share): an online merge,
+        // one piece's row in flight at a time
+        float acc[D];
+#pragma unroll
+        for (int e = 0; e < D; ++e) acc[e] = 0.f;
+        float mx = -INFINITY, wsum = 0.f;
+        for (int i = 0; i < total; ++i) {
+          const size_t pr = static_cast<size_t>(list_t[i]) + prow;
+          const float li = __ldcg(p.part_lse + pr);
+          const uint4* src = reinterpret_cast<const uint4*>(p.part_o + pr * D);
+          uint4 v[kChunks];
+#pragma unroll
+          for (int ch = 0; ch < kChunks; ++ch) v[ch] = __ldcg(src + ch);
+          if (li == -INFINITY) continue;
+          if (li > mx) {
+            const float f = (mx == -INFINITY) ? 0.f : ex2(mx - li);
+            wsum *= f;
+#pragma unroll
+            for (int e = 0; e < D; ++e) acc[e] *= f;
+            mx = li;
+          }
+          const float w = ex2(li - mx);
+          wsum += w;
+#pragma unroll
+          for (int ch = 0; ch < kChunks; ++ch) {
+            const uint32_t x[4] = {v[ch].x, v[ch].y, v[ch].z, v[ch].w};
+#pragma unroll
+            for (int k2 = 0; k2 < 4; ++k2) {
+              acc[ch * 8 + 2 * k2] += w * __uint_as_float(x[k2] << 16);
+              acc[ch * 8 + 2 * k2 + 1] += w * __uint_as_float(x[k2] & 0xFFFF0000u);
+            }
+          }
+        }
+        const float inv = (wsum > 0.f) ? 1.f / wsum : 0.f;
+#pragma unroll
+        for (int ch = 0; ch < kChunks; ++ch)
+          dst[ch] = make_uint4(pack_bf16x2(acc[ch * 8 + 0] * inv, acc[ch * 8 + 1] * inv),
+                               pack_bf16x2(acc[ch * 8 + 2] * inv, acc[ch * 8 + 3] * inv),
+                               pack_bf16x2(acc[ch * 8 + 4] * inv, acc[ch * 8 + 5] * inv),
+                               pack_bf16x2(acc[ch * 8 + 6] * inv, acc[ch * 8 + 7] * inv));
+        if (p.lse != nullptr) p.lse[orow] = (wsum > 0.f) ? (mx + log2f(wsum)) * kLn2 : -INFINITY;
+      }
     }
     if (!ok && lane == 0) {
       report_error(p.err, SV_DEVERR_TIMEOUT);

@@ -11,14 +11,15 @@
 //
 //   * Rows r = node * G + g; two 128-row M tiles per CTA, Q of both in shared
 //     memory; K/V pages (16 tokens, head-major inside a page) gathered by TMA,
-//     eight pages per 128-key tile, 128-byte swizzled, into two K and two V
-//     stages (D = 128) or four (D = 64); the tree's K/V are one extra tile.
+//     eight pages per 128-key tile, 128-byte swizzled, into three K and two V
+//     stages (D = 128) or five of each (D = 64); the tree's K/V are one extra
+//     tile.
 //   * tcgen05.mma: S = Q K^T into TMEM (S0, S1), P written back as bf16 into
 //     the S columns, O += P V (O0, O1) — the 512 TMEM columns.  MMA order
 //     S0 S1 | PV0 S0' | PV1 S1' ... so the two softmax groups alternate.
-//   * Warp roles: warp 0 loads (TMA), warp 1 issues MMAs (one thread), warps
-//     4-7 and 8-11 run the softmax of the two row tiles; setmaxnreg moves
-//     registers to the softmax groups.
+//   * Warp roles: warp 0 loads Q and the K tiles, warp 3 the V tiles (TMA),
+//     warp 1 issues MMAs (one thread), warps 4-7 and 8-11 run the softmax of
+//     the two row tiles; setmaxnreg moves registers to the softmax groups.
 //   * KV splits write partials (O / l in bf16 and log2-sum-exp) that the
 //     combine kernel of tree_attention.cu merges.
 #include <math.h>
@@ -47,14 +48,17 @@ enum ReduceMode : int { kReduceNone = 0, kReduceGlobal = 2 };
 template <int D>
 struct Cfg {
   static constexpr int kHalves = D / 64;                   // 128-byte column halves
-  static constexpr int kStages = (D == 128) ? 2 : 4;
+  // K stages return to the loader once their QK^T is done, V stages only
+  // after PV: K may run a stage further ahead
+  static constexpr int kKStages = (D == 128) ? 3 : 5;
+  static constexpr int kVStages = (D == 128) ? 2 : 5;
   static constexpr uint32_t kHalfBytes = 128u * 128u;      // 128 rows x 128 B
   static constexpr uint32_t kQTileBytes = kTileRows * D * 2;
   static constexpr uint32_t kKVTileBytes = kBlockN * D * 2;
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffK = kOffQ + 2 * kQTileBytes;
-  static constexpr uint32_t kOffV = kOffK + kStages * kKVTileBytes;
-  static constexpr uint32_t kOffBar = kOffV + kStages * kKVTileBytes;
+  static constexpr uint32_t kOffV = kOffK + kKStages * kKVTileBytes;
+  static constexpr uint32_t kOffBar = kOffV + kVStages * kKVTileBytes;
   static constexpr uint32_t kBarBytes = 512;
   static constexpr uint32_t kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
@@ -65,6 +69,7 @@ struct Cfg {
   static constexpr uint32_t kStageStride = D * 4 + 16;
   static constexpr uint32_t kOffStage = 0;
   static_assert(kOffStage + 2 * kTileRows * kStageStride <= kOffBar, "staging must fit below the barriers");
+  static_assert(kOffBar + kBarBytes + 1024 <= 232448, "shared memory per CTA");
 };
 
 struct Params {
@@ -98,7 +103,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                           const __grid_constant__ CUtensorMap tm_vc, const __grid_constant__ CUtensorMap tm_tk,
                           const __grid_constant__ CUtensorMap tm_tv, const __grid_constant__ Params p) {
   using C = Cfg<D>;
-  constexpr int NST = C::kStages;
+  constexpr int NSK = C::kKStages;
+  constexpr int NSV = C::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -128,10 +134,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
-  uint64_t* v_full = k_full + NST;
-  uint64_t* k_empty = v_full + NST;
-  uint64_t* v_empty = k_empty + NST;
-  uint64_t* s_full = v_empty + NST;  // [2]
+  uint64_t* v_full = k_full + NSK;
+  uint64_t* k_empty = v_full + NSV;
+  uint64_t* v_empty = k_empty + NSK;
+  uint64_t* s_full = v_empty + NSV;  // [2]
   uint64_t* p_full = s_full + 2;     // [2]
   uint64_t* o_final = p_full + 2;    // [2]
   uint64_t* drain = o_final + 2;
@@ -142,10 +148,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- prologue that reads no input: it may overlap the previous grid
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < NST; ++i) {
+    for (int i = 0; i < NSK; ++i) {
       mbar_init(k_full + i, 1);
-      mbar_init(v_full + i, 1);
       mbar_init(k_empty + i, 1);
+    }
+    for (int i = 0; i < NSV; ++i) {
+      mbar_init(v_full + i, 1);
       mbar_init(v_empty + i, 1);
     }
     for (int t = 0; t < 2; ++t) {
@@ -220,11 +228,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < 4) {
     regs_decrease<kRegsControl>();
-    if (work && warp == 0) {
-      // ------------------------------------------------------------ producer
-      int k_issued = 0, v_issued = 0;
+    if (work && (warp == 0 || warp == 3)) {
+      // ------------------------------------------------------------ loaders
+      // warp 0 loads Q and the K tiles, warp 3 the V tiles, each as far ahead
+      // as its ring allows (both resolve the tiles' page ids)
+      const bool is_k = warp == 0;
+      const int NS = is_k ? NSK : NSV;
+      uint64_t* full = is_k ? k_full : v_full;
+      uint64_t* empty = is_k ? k_empty : v_empty;
+      uint8_t* ring = smem + (is_k ? C::kOffK : C::kOffV);
+      const CUtensorMap* tm_cache = is_k ? &tm_kc : &tm_vc;
+      const CUtensorMap* tm_tree = is_k ? &tm_tk : &tm_tv;
+      int issued = 0;
       bool ok = true;
-      if (lane == 0) {
+      if (is_k && lane == 0) {
         mbar_arrive_expect_tx(q_full, (tile1 ? 2u : 1u) * C::kQTileBytes);
         for (int t = 0; t < (tile1 ? 2 : 1); ++t)
           for (int h = 0; h < C::kHalves; ++h)
@@ -233,8 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int it = 0; it < ntiles; ++it) {
         const int j = jb + it;
-        const int st = it % NST;
-        const uint32_t ph = (it / NST) & 1;
+        const int st = it % NS;
+        const uint32_t ph = (it / NS) & 1;
         const bool ctx = j < t_ctx;
         int phys = 0;
         if (ctx && lane < kPagesPerTile) {
@@ -250,48 +267,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             phys = 0;
           }
         }
-        // K tile
-        if (it >= NST) {
-          int w = (lane == 0) ? (mbar_wait(k_empty + st, ph ^ 1u, abort_flag) ? 1 : 0) : 0;
+        if (it >= NS) {
+          int w = (lane == 0) ? (mbar_wait(empty + st, ph ^ 1u, abort_flag) ? 1 : 0) : 0;
           if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
         }
-        if (lane == 0) mbar_arrive_expect_tx(k_full + st, C::kKVTileBytes);
+        if (lane == 0) mbar_arrive_expect_tx(full + st, C::kKVTileBytes);
         __syncwarp();
-        uint8_t* kdst = smem + C::kOffK + st * C::kKVTileBytes;
+        uint8_t* dst = ring + st * C::kKVTileBytes;
         if (ctx) {
           if (lane < kPagesPerTile)
             for (int h = 0; h < C::kHalves; ++h)
-              tma_load_4d(kdst + h * C::kHalfBytes + lane * 2048, &tm_kc, k_full + st, h * 64, 0, kh, phys);
+              tma_load_4d(dst + h * C::kHalfBytes + lane * 2048, tm_cache, full + st, h * 64, 0, kh, phys);
         } else if (lane == 0) {
-          for (int h = 0; h < C::kHalves; ++h) tma_load_3d(kdst + h * C::kHalfBytes, &tm_tk, k_full + st, h * 64, kh, n0);
+          for (int h = 0; h < C::kHalves; ++h) tma_load_3d(dst + h * C::kHalfBytes, tm_tree, full + st, h * 64, kh, n0);
         }
-        k_issued = it + 1;
-        // V tile
-        if (it >= NST) {
-          int w = (lane == 0) ? (mbar_wait(v_empty + st, ph ^ 1u, abort_flag) ? 1 : 0) : 0;
-          if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
-        }
-        if (lane == 0) mbar_arrive_expect_tx(v_full + st, C::kKVTileBytes);
-        __syncwarp();
-        uint8_t* vdst = smem + C::kOffV + st * C::kKVTileBytes;
-        if (ctx) {
-          if (lane < kPagesPerTile)
-            for (int h = 0; h < C::kHalves; ++h)
-              tma_load_4d(vdst + h * C::kHalfBytes + lane * 2048, &tm_vc, v_full + st, h * 64, 0, kh, phys);
-        } else if (lane == 0) {
-          for (int h = 0; h < C::kHalves; ++h) tma_load_3d(vdst + h * C::kHalfBytes, &tm_tv, v_full + st, h * 64, kh, n0);
-        }
-        v_issued = it + 1;
+        issued = it + 1;
       }
       if (!ok && lane == 0) {
         // Timed out: stop the other roles, then let our copies land before exit.
         report_error(p.err, SV_DEVERR_TIMEOUT);
         *abort_flag = 1;
-        mbar_wait(q_full, 0, never_set);
-        for (int it = max(0, k_issued - NST); it < k_issued; ++it)
-          mbar_wait(k_full + (it % NST), (it / NST) & 1, never_set);
-        for (int it = max(0, v_issued - NST); it < v_issued; ++it)
-          mbar_wait(v_full + (it % NST), (it / NST) & 1, never_set);
+        if (is_k) mbar_wait(q_full, 0, never_set);
+        for (int it = max(0, issued - NS); it < issued; ++it) mbar_wait(full + (it % NS), (it / NS) & 1, never_set);
       }
     } else if (work && warp == 1) {
       // ------------------------------------------------------------ MMA issuer
@@ -333,16 +330,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(k_empty);
         }
         for (int it = 0; ok && it < ntiles; ++it) {
-          const int st = it % NST;
-          const uint32_t ph = (it / NST) & 1;
+          const int vst = it % NSV;
+          const uint32_t vph = (it / NSV) & 1;
           const int nx = it + 1;
-          const int st2 = nx % NST;
-          const uint32_t ph2 = (nx / NST) & 1;
-          if (!mbar_wait(v_full + st, ph, abort_flag)) { ok = false; break; }
+          const int st2 = nx % NSK;
+          const uint32_t ph2 = (nx / NSK) & 1;
+          if (!mbar_wait(v_full + vst, vph, abort_flag)) { ok = false; break; }
           for (int t = 0; t < nt; ++t) {
             if (!mbar_wait(p_full + t, it & 1, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            issue_pv(t, st, it > 0);
+            issue_pv(t, vst, it > 0);
             if (nx < ntiles) {
               if (t == 0) {
                 if (!mbar_wait(k_full + st2, ph2, abort_flag)) { ok = false; break; }
@@ -353,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!ok) break;
-          umma_commit(v_empty + st);
+          umma_commit(v_empty + vst);
           if (nx < ntiles) umma_commit(k_empty + st2);
         }
         if (ok) {
