@@ -374,6 +374,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = row0 + r_cta;
     const bool row_exists = row < rows_total;
     const bool active = work && (t == 0 || tile1);  // warp-uniform
+    // A warp whose 32 rows are all past the tree's rows only keeps the
+    // barrier protocol (its S and P columns are never read back into an
+    // output), which frees its scheduler's issue slots for the other warp.
+    const bool warp_rows = __any_sync(0xffffffffu, row_exists);
     const int node = row / G;
     const int g = row - node * G;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(qw * 32) << 16);
@@ -409,6 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int j = jb + it;
           // warp-uniform outcome: the TMEM loads below are warp-collective
           if (!__all_sync(0xffffffffu, mbar_wait(s_full + t, it & 1, abort_flag))) { ok = false; break; }
+          if (!warp_rows) {
+            mbar_arrive(p_full + t);
+            continue;
+          }
           tc_fence_after();
           if (it == 0 && t == 0 && r == 0) mark(SV_TRACE_FIRST_S);
           uint32_t sr[kBlockN];
@@ -506,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------------------------------------------------- epilogue
-    const bool have_o = active && ok;  // warp-uniform
+    const bool have_o = active && ok && warp_rows;  // warp-uniform
     if (have_o) tc_fence_after();
     const float inv_l = (l_run > 0.f) ? 1.f / l_run : 0.f;
     const float lse2 = (have_o && l_run > 0.f) ? m_run + log2f(l_run) : -INFINITY;
