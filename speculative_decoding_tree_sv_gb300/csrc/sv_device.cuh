@@ -212,6 +212,21 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       : "memory");
 }
 
+// True on one lane of the warp (the lowest active one; lane 0 of a converged
+// warp).  The MMA warps run their whole schedule converged, so descriptors and
+// loop state stay warp-uniform, and issue each tcgen05.mma / commit from the
+// lane this elects: the same lane every time, which the commit's "all prior
+// ops of this thread" needs.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // Arrive (once) on `bar` when all previously issued tcgen05 async ops of
 // this thread have completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {

@@ -403,82 +403,97 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (work && warp == 1) {
       // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
-        constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kBlockN, false, false);
-        constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
-        const uint32_t k_base = smem_u32(smem + C::kOffK);
-        const uint32_t v_base = smem_u32(smem + C::kOffV);
-        // S = Q K^T: Q (bf16 pairs) from TMEM, K K-major from shared memory
-        auto issue_qk = [&](int buf, int kst) {
-          const uint32_t d = tmem + (buf ? C::kColS1 : C::kColS0);
+      // The whole warp runs the schedule, so descriptors and loop state stay
+      // warp-uniform; one elected lane issues each MMA and commit.  (Issuing
+      // from a lane-0-only branch cost about three times the MMA's own time
+      // per instruction.)
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kBlockN, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+      const uint32_t k_base = smem_u32(smem + C::kOffK);
+      const uint32_t v_base = smem_u32(smem + C::kOffV);
+      auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+      };
+      auto commit = [&](uint64_t* bar) {
+        if (elect_one()) umma_commit(bar);
+        __syncwarp();
+      };
+      // S = Q K^T: Q (bf16 pairs) from TMEM, K K-major from shared memory
+      auto issue_qk = [&](int buf, int kst) {
+        const uint32_t d = tmem + (buf ? C::kColS1 : C::kColS0);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-            const uint64_t bdesc = smem_desc_sw128(k_base + kst * C::kTileBytes + off, 16, 1024);
-            umma_ts(d, tmem + C::kColQ + kk * 8, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
-          }
-        };
-        // O += P V: P (bf16 pairs) in the score buffer's first columns
-        auto issue_pv = [&](int buf, int vst, bool accumulate) {
-          const uint32_t d = tmem + C::kColO;
-          const uint32_t a = tmem + (buf ? C::kColS1 : C::kColS0);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
+          const uint64_t bdesc = smem_desc_sw128(k_base + kst * C::kTileBytes + off, 16, 1024);
+          if (elect_one()) umma_ts(d, tmem + C::kColQ + kk * 8, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+          __syncwarp();
+        }
+      };
+      // O += P V: P (bf16 pairs) in the score buffer's first columns
+      auto issue_pv = [&](int buf, int vst, bool accumulate) {
+        const uint32_t d = tmem + C::kColO;
+        const uint32_t a = tmem + (buf ? C::kColS1 : C::kColS0);
 #pragma unroll
-          for (int kk = 0; kk < kBlockN / 16; ++kk) {
-            const uint64_t bdesc = smem_desc_sw128(v_base + vst * C::kTileBytes + kk * 2048, C::kHalfBytes, 1024);
-            umma_ts(d, a + kk * 8, bdesc, idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
-          }
-        };
-        // A stage goes back to the loaders of both CTAs of a pair once this
-        // CTA's MMAs have read it.  The last stages of a ring are never
-        // refilled, so they are not released: no arrive is left in flight
-        // towards the peer when the CTAs finish.
-        auto release = [&](uint64_t* bar, int it, int ns) {
-          if (it + ns < ntiles) {
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          const uint64_t bdesc = smem_desc_sw128(v_base + vst * C::kTileBytes + kk * 2048, C::kHalfBytes, 1024);
+          if (elect_one()) umma_ts(d, a + kk * 8, bdesc, idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
+          __syncwarp();
+        }
+      };
+      // A stage goes back to the loaders of both CTAs of a pair once this
+      // CTA's MMAs have read it.  The last stages of a ring are never
+      // refilled, so they are not released: no arrive is left in flight
+      // towards the peer when the CTAs finish.
+      auto release = [&](uint64_t* bar, int it, int ns) {
+        if (it + ns < ntiles) {
+          if (elect_one()) {
             if (paired) umma_commit_mc(bar, kPairMask);
             else umma_commit(bar);
           }
-        };
-        bool ok = mbar_wait(q_full, 0, abort_flag);
-        // scores of the first two tiles, one per buffer
-        for (int it = 0; ok && it < 2 && it < ntiles; ++it) {
-          if (!mbar_wait(k_full + it % NSK, (it / NSK) & 1, abort_flag)) { ok = false; break; }
-          tc_fence_after();
-          if (it == 0) mark(SV_TRACE_FIRST_MMA);
-          issue_qk(it, it % NSK);
-          umma_commit(s_full + it);
-          release(k_empty + it % NSK, it, NSK);
+          __syncwarp();
         }
-        for (int it = 0; ok && it < ntiles; ++it) {
-          const int buf = it & 1;
-          const int vst = it % NSV;
-          if (!mbar_wait(v_full + vst, (it / NSV) & 1, abort_flag)) { ok = false; break; }
-          if (!mbar_wait(p_full + buf, (it >> 1) & 1, abort_flag)) { ok = false; break; }
+      };
+      bool ok = wait_all(q_full, 0);
+      // scores of the first two tiles, one per buffer
+      for (int it = 0; ok && it < 2 && it < ntiles; ++it) {
+        if (!wait_all(k_full + it % NSK, (it / NSK) & 1)) { ok = false; break; }
+        tc_fence_after();
+        if (it == 0 && lane == 0) mark(SV_TRACE_FIRST_MMA);
+        issue_qk(it, it % NSK);
+        commit(s_full + it);
+        release(k_empty + it % NSK, it, NSK);
+      }
+      for (int it = 0; ok && it < ntiles; ++it) {
+        const int buf = it & 1;
+        const int vst = it % NSV;
+        if (!wait_all(v_full + vst, (it / NSV) & 1)) { ok = false; break; }
+        if (!wait_all(p_full + buf, (it >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        issue_pv(buf, vst, it > 0);
+        commit(pv_done);
+        release(v_empty + vst, it, NSV);
+        // the next scores of this buffer overwrite P(it) after PV(it) has
+        // read it: tcgen05 MMAs of one thread execute in issue order
+        const int nx = it + 2;
+        if (nx < ntiles) {
+          const int kst = nx % NSK;
+          if (!wait_all(k_full + kst, (nx / NSK) & 1)) { ok = false; break; }
           tc_fence_after();
-          issue_pv(buf, vst, it > 0);
-          umma_commit(pv_done);
-          release(v_empty + vst, it, NSV);
-          // the next scores of this buffer overwrite P(it) after PV(it) has
-          // read it: tcgen05 MMAs of one thread execute in issue order
-          const int nx = it + 2;
-          if (nx < ntiles) {
-            const int kst = nx % NSK;
-            if (!mbar_wait(k_full + kst, (nx / NSK) & 1, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            issue_qk(buf, kst);
-            umma_commit(s_full + buf);
-            release(k_empty + kst, nx, NSK);
-          }
-        }
-        if (ok) {
-          umma_commit(o_final);
-        } else {
-          report_error(p.err, SV_DEVERR_TIMEOUT);
-          *abort_flag = 1;
-          umma_commit(drain);  // let issued MMAs finish before TMEM is freed
-          mbar_wait(drain, 0, never_set);
+          issue_qk(buf, kst);
+          commit(s_full + buf);
+          release(k_empty + kst, nx, NSK);
         }
       }
-      __syncwarp();
+      if (ok) {
+        commit(o_final);
+      } else {
+        if (lane == 0) {
+          report_error(p.err, SV_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        commit(drain);  // let issued MMAs finish before TMEM is freed
+        __all_sync(0xffffffffu, mbar_wait(drain, 0, never_set));
+      }
     }
   } else {
     // ------------------------------------------------------------ softmax

@@ -523,7 +523,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     } else if (warp == 1) {
       // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
+      // The whole warp runs the schedule (warp-uniform descriptors and loop
+      // state); one elected lane issues each MMA and commit.
+      {
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+          return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+        };
+        auto commit = [&](uint64_t* bar) {
+          if (elect_one()) umma_commit(bar);
+          __syncwarp();
+        };
         constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kBlockN, false, false);
         constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
         const uint32_t q_base = smem_u32(smem + C::kOffQ);
@@ -536,7 +545,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
             const uint64_t a = smem_desc_sw128(q_base + t * C::kQTileBytes + off, 16, 1024);
             const uint64_t bdesc = smem_desc_sw128(k_base + st * C::kKVTileBytes + off, 16, 1024);
-            umma_ss(d, a, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+            if (elect_one()) umma_ss(d, a, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+            __syncwarp();
           }
         };
         auto issue_pv = [&](int t, int st, bool accumulate) {
@@ -545,7 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kBlockN / 16; ++kk) {
             const uint64_t bdesc = smem_desc_sw128(v_base + st * C::kKVTileBytes + kk * 2048, C::kHalfBytes, 1024);
-            umma_ts(d, a + kk * 8, bdesc, idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
+            if (elect_one()) umma_ts(d, a + kk * 8, bdesc, idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
+            __syncwarp();
           }
         };
         Cursor cur = cur0;
@@ -554,21 +565,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         int g = 0;                // ring position of the piece's first tile
         int tiles_t[2] = {0, 0};  // tiles handed to each M tile's softmax before this piece
         for (int k = 0; ok; ++k) {
-          if (k == 1 && !mbar_wait(list_ready, 0, abort_flag)) { ok = false; break; }
+          if (k == 1 && !wait_all(list_ready, 0)) { ok = false; break; }
           if (!get_piece(p, k, cur, pc, list, nlist, cont)) break;
           const int nt = pc.nt;
           const int n = pc.je - pc.ja;
           const int st0 = g % NST;
-          ok = mbar_wait(q_full, k & 1, abort_flag) && mbar_wait(k_full + st0, (g / NST) & 1, abort_flag);
+          ok = wait_all(q_full, k & 1) && wait_all(k_full + st0, (g / NST) & 1);
           if (!ok) break;
           tc_fence_after();
-          if (k == 0) mark(SV_TRACE_FIRST_MMA);
+          if (k == 0 && lane == 0) mark(SV_TRACE_FIRST_MMA);
           for (int t = 0; t < nt; ++t) {
             issue_qk(t, st0);
-            umma_commit(s_full + t);
+            commit(s_full + t);
           }
-          umma_commit(k_empty + st0);
-          if (n == 1) umma_commit(q_empty);  // the piece's last QK^T is issued
+          commit(k_empty + st0);
+          if (n == 1) commit(q_empty);  // the piece's last QK^T is issued
           for (int it = 0; ok && it < n; ++it) {
             const int gg = g + it;
             const int st = gg % NST;
@@ -576,37 +587,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nx = it + 1;
             const int st2 = (gg + 1) % NST;
             const uint32_t ph2 = ((gg + 1) / NST) & 1;
-            if (!mbar_wait(v_full + st, ph, abort_flag)) { ok = false; break; }
+            if (!wait_all(v_full + st, ph)) { ok = false; break; }
             for (int t = 0; t < nt; ++t) {
-              if (!mbar_wait(p_full + t, (tiles_t[t] + it) & 1, abort_flag)) { ok = false; break; }
+              if (!wait_all(p_full + t, (tiles_t[t] + it) & 1)) { ok = false; break; }
               tc_fence_after();
               issue_pv(t, st, it > 0);
               if (nx < n) {
                 if (t == 0) {
-                  if (!mbar_wait(k_full + st2, ph2, abort_flag)) { ok = false; break; }
+                  if (!wait_all(k_full + st2, ph2)) { ok = false; break; }
                   tc_fence_after();
                 }
                 issue_qk(t, st2);
-                umma_commit(s_full + t);
+                commit(s_full + t);
               }
             }
             if (!ok) break;
-            umma_commit(v_empty + st);
+            commit(v_empty + st);
             if (nx < n) {
-              umma_commit(k_empty + st2);
-              if (nx == n - 1) umma_commit(q_empty);
+              commit(k_empty + st2);
+              if (nx == n - 1) commit(q_empty);
             }
           }
           if (!ok) break;
-          for (int t = 0; t < nt; ++t) umma_commit(o_final + t);
+          for (int t = 0; t < nt; ++t) commit(o_final + t);
           g += n;
           for (int t = 0; t < nt; ++t) tiles_t[t] += n;
         }
         if (!ok) {
-          report_error(p.err, SV_DEVERR_TIMEOUT);
-          *abort_flag = 1;
-          umma_commit(drain);  // let issued MMAs finish before TMEM is freed
-          mbar_wait(drain, 0, never_set);
+          if (lane == 0) {
+            report_error(p.err, SV_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+          }
+          commit(drain);  // let issued MMAs finish before TMEM is freed
+          __all_sync(0xffffffffu, mbar_wait(drain, 0, never_set));
         }
       }
       __syncwarp();

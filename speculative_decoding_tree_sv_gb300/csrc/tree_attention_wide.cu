@@ -292,77 +292,89 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (work && warp == 1) {
       // ------------------------------------------------------------ MMA issuer
-      if (lane == 0) {
-        constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kBlockN, false, false);
-        constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
-        const int nt = tile1 ? 2 : 1;
-        const uint32_t q_base = smem_u32(smem + C::kOffQ);
-        const uint32_t k_base = smem_u32(smem + C::kOffK);
-        const uint32_t v_base = smem_u32(smem + C::kOffV);
-        bool ok = mbar_wait(q_full, 0, abort_flag);
-        auto issue_qk = [&](int t, int st) {
-          const uint32_t d = tmem + (t ? C::kColS1 : C::kColS0);
+      // The whole warp runs the schedule, so descriptors and loop state stay
+      // warp-uniform; one elected lane issues each MMA and commit.  (Issuing
+      // from a lane-0-only branch cost about three times the MMA's own time
+      // per instruction.)
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, kBlockN, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, D, false, true);
+      const int nt = tile1 ? 2 : 1;
+      const uint32_t q_base = smem_u32(smem + C::kOffQ);
+      const uint32_t k_base = smem_u32(smem + C::kOffK);
+      const uint32_t v_base = smem_u32(smem + C::kOffV);
+      auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+      };
+      auto commit = [&](uint64_t* bar) {
+        if (elect_one()) umma_commit(bar);
+        __syncwarp();
+      };
+      auto issue_qk = [&](int t, int st) {
+        const uint32_t d = tmem + (t ? C::kColS1 : C::kColS0);
   #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-            const uint64_t a = smem_desc_sw128(q_base + t * C::kQTileBytes + off, 16, 1024);
-            const uint64_t bdesc = smem_desc_sw128(k_base + st * C::kKVTileBytes + off, 16, 1024);
-            umma_ss(d, a, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
-          }
-        };
-        auto issue_pv = [&](int t, int st, bool accumulate) {
-          const uint32_t d = tmem + (t ? C::kColO1 : C::kColO0);
-          const uint32_t a = tmem + (t ? C::kColS1 : C::kColS0);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
+          const uint64_t a = smem_desc_sw128(q_base + t * C::kQTileBytes + off, 16, 1024);
+          const uint64_t bdesc = smem_desc_sw128(k_base + st * C::kKVTileBytes + off, 16, 1024);
+          if (elect_one()) umma_ss(d, a, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+          __syncwarp();
+        }
+      };
+      auto issue_pv = [&](int t, int st, bool accumulate) {
+        const uint32_t d = tmem + (t ? C::kColO1 : C::kColO0);
+        const uint32_t a = tmem + (t ? C::kColS1 : C::kColS0);
   #pragma unroll
-          for (int kk = 0; kk < kBlockN / 16; ++kk) {
-            const uint64_t bdesc = smem_desc_sw128(v_base + st * C::kKVTileBytes + kk * 2048, C::kHalfBytes, 1024);
-            umma_ts(d, a + kk * 8, bdesc, idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
-          }
-        };
-        if (ok) ok = mbar_wait(k_full, 0, abort_flag);
-        if (ok) {
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          const uint64_t bdesc = smem_desc_sw128(v_base + st * C::kKVTileBytes + kk * 2048, C::kHalfBytes, 1024);
+          if (elect_one()) umma_ts(d, a + kk * 8, bdesc, idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
+          __syncwarp();
+        }
+      };
+      bool ok = wait_all(q_full, 0);
+      if (ok) ok = wait_all(k_full, 0);
+      if (ok) {
+        tc_fence_after();
+        if (lane == 0) mark(SV_TRACE_FIRST_MMA);
+        for (int t = 0; t < nt; ++t) {
+          issue_qk(t, 0);
+          commit(s_full + t);
+        }
+        commit(k_empty);
+      }
+      for (int it = 0; ok && it < ntiles; ++it) {
+        const int vst = it % NSV;
+        const uint32_t vph = (it / NSV) & 1;
+        const int nx = it + 1;
+        const int st2 = nx % NSK;
+        const uint32_t ph2 = (nx / NSK) & 1;
+        if (!wait_all(v_full + vst, vph)) { ok = false; break; }
+        for (int t = 0; t < nt; ++t) {
+          if (!wait_all(p_full + t, it & 1)) { ok = false; break; }
           tc_fence_after();
-          mark(SV_TRACE_FIRST_MMA);
-          for (int t = 0; t < nt; ++t) {
-            issue_qk(t, 0);
-            umma_commit(s_full + t);
-          }
-          umma_commit(k_empty);
-        }
-        for (int it = 0; ok && it < ntiles; ++it) {
-          const int vst = it % NSV;
-          const uint32_t vph = (it / NSV) & 1;
-          const int nx = it + 1;
-          const int st2 = nx % NSK;
-          const uint32_t ph2 = (nx / NSK) & 1;
-          if (!mbar_wait(v_full + vst, vph, abort_flag)) { ok = false; break; }
-          for (int t = 0; t < nt; ++t) {
-            if (!mbar_wait(p_full + t, it & 1, abort_flag)) { ok = false; break; }
-            tc_fence_after();
-            issue_pv(t, vst, it > 0);
-            if (nx < ntiles) {
-              if (t == 0) {
-                if (!mbar_wait(k_full + st2, ph2, abort_flag)) { ok = false; break; }
-                tc_fence_after();
-              }
-              issue_qk(t, st2);
-              umma_commit(s_full + t);
+          issue_pv(t, vst, it > 0);
+          if (nx < ntiles) {
+            if (t == 0) {
+              if (!wait_all(k_full + st2, ph2)) { ok = false; break; }
+              tc_fence_after();
             }
+            issue_qk(t, st2);
+            commit(s_full + t);
           }
-          if (!ok) break;
-          umma_commit(v_empty + vst);
-          if (nx < ntiles) umma_commit(k_empty + st2);
         }
-        if (ok) {
-          for (int t = 0; t < nt; ++t) umma_commit(o_final + t);
-        } else {
+        if (!ok) break;
+        commit(v_empty + vst);
+        if (nx < ntiles) commit(k_empty + st2);
+      }
+      if (ok) {
+        for (int t = 0; t < nt; ++t) commit(o_final + t);
+      } else {
+        if (lane == 0) {
           report_error(p.err, SV_DEVERR_TIMEOUT);
           *abort_flag = 1;
-          umma_commit(drain);  // let issued MMAs finish before TMEM is freed
-          mbar_wait(drain, 0, never_set);
         }
+        commit(drain);  // let issued MMAs finish before TMEM is freed
+        __all_sync(0xffffffffu, mbar_wait(drain, 0, never_set));
       }
-      __syncwarp();
     }
   } else {
     regs_increase<kRegsSoftmax>();
