@@ -30,8 +30,9 @@
 //     tcgen05.mma accumulates O += P V (P from TMEM, V MN-major in smem).
 //     TMEM columns: S0, S1, O, Q.  MMA order: S0 S1 | PV0 S2 | PV1 S3 | ...
 //   * Warp roles: warp 0 loads the K tiles, warp 3 the V tiles, warp 2
-//     resolves page ids ahead of them, warp 1 issues MMAs (one thread),
-//     warps 4-7 load Q, run the softmax and the epilogue.
+//     resolves page ids ahead of them, warp 1 runs the MMA schedule
+//     (converged; one elected lane issues each MMA and commit), warps 4-7
+//     load Q, run the softmax and the epilogue.
 //   * KV splits write partials (O / l in bf16 and log2-sum-exp) to the
 //     workspace; a combine kernel merges them.
 //   * Launches allow programmatic dependent launch: the prologue (barriers,

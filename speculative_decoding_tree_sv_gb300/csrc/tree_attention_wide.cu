@@ -18,8 +18,9 @@
 //     the S columns, O += P V (O0, O1) — the 512 TMEM columns.  MMA order
 //     S0 S1 | PV0 S0' | PV1 S1' ... so the two softmax groups alternate.
 //   * Warp roles: warp 0 loads Q and the K tiles, warp 3 the V tiles (TMA),
-//     warp 1 issues MMAs (one thread), warps 4-7 and 8-11 run the softmax of
-//     the two row tiles; setmaxnreg moves registers to the softmax groups.
+//     warp 1 runs the MMA schedule (converged; one elected lane issues each
+//     MMA and commit), warps 4-7 and 8-11 run the softmax of the two row
+//     tiles; setmaxnreg moves registers to the softmax groups.
 //   * KV splits write partials (O / l in bf16 and log2-sum-exp) that the
 //     combine kernel of tree_attention.cu merges.
 #include <math.h>
