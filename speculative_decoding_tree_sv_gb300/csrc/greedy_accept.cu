@@ -16,10 +16,11 @@
 // folds its (value, index) maximum into a per-row 64-bit key with atomicMax
 // (order-preserving float bits in the high word, inverted index in the low
 // word, so the lowest index wins ties).  The last CTA to finish a sequence
-// (atomic ticket, no waiting) walks that sequence's tree with all its
-// threads, one node per thread: pointer jumping gives every node its depth,
-// its accepted flag and its ancestor set in at most log2(128) rounds, then a
-// short top-down walk picks the lexicographically smallest deepest path.  It
+// (atomic ticket, no waiting) walks that sequence's tree: its threads load
+// one node each, then one warp (four nodes per lane, warp syncs only) jumps
+// pointers, which gives every node its depth, its accepted flag and its
+// ancestor set in at most log2(128) rounds, and a short top-down walk picks
+// the lexicographically smallest deepest path.  It
 // resets the keys and the ticket so the workspace is ready for the next call.
 //
 // Rows that do not start on a 16-byte boundary (vocabulary not a multiple of
@@ -83,8 +84,9 @@ __device__ void write_no_tree(const Params& p, int b) {
   }
 }
 
-// Tree walk of sequence b (nodes n0 .. n0 + N - 1) by the whole CTA, one node
-// per thread; `scratch` is 8 KB of shared memory nothing else uses now.
+// Tree walk of sequence b (nodes n0 .. n0 + N - 1): the CTA loads the nodes
+// (one per thread), then one warp jumps pointers and walks; `scratch` is 8 KB
+// of shared memory nothing else uses now.
 __device__ void walk_sequence(const Params& p, int b, int n0, int N, uint8_t* scratch) {
   int* s_am = reinterpret_cast<int*>(scratch);                  // [128]
   int* s_par = s_am + kMaxNodes;                                // [128]
@@ -92,8 +94,6 @@ __device__ void walk_sequence(const Params& p, int b, int n0, int N, uint8_t* sc
   int* s_dep = s_ptr + 2 * kMaxNodes;                           // [2][128]
   uint32_t* s_acc = reinterpret_cast<uint32_t*>(s_dep + 2 * kMaxNodes);  // [2][128]
   uint32_t* s_anc = s_acc + 2 * kMaxNodes;                      // [2][128][4]
-  uint32_t* s_good = s_anc + 2 * kMaxNodes * 4;                 // [4]
-  int* s_best = reinterpret_cast<int*>(s_good + 4);
   const int t = threadIdx.x;
   if (N < 1 || N > kMaxNodes) {  // uniform over the CTA
     // no walk: the keys go back to zero for the next call on this
@@ -103,8 +103,6 @@ __device__ void walk_sequence(const Params& p, int b, int n0, int N, uint8_t* sc
     if (t == 0) p.tickets[b] = 0;
     return;
   }
-  if (t < 4) s_good[t] = 0u;
-  if (t == 0) *s_best = 0;
   int am = 0, par = -1, tok = 0;
   if (t < N) {
     // the keys were last written by atomics at L2: read them there, then reset
@@ -136,42 +134,65 @@ __device__ void walk_sequence(const Params& p, int b, int n0, int N, uint8_t* sc
     }
     if (p.argmax_out != nullptr) p.argmax_out[n0 + t] = am;
   }
+  __syncthreads();
+  if (t >= 32) return;
+  // The rest is one warp's (lane owns nodes lane + 32 s): warp syncs instead
+  // of block barriers keep each round a few hundred cycles shorter.
+  const int lane = t;
   // pointer jumping: after round r, ptr = 2^(r+1)-th ancestor (clamped at
   // the root), dep = distance to it, acc = all matched on the way, anc =
   // every node within that distance; done once every pointer is the root
   int cur = 0;
   for (int round = 0;; ++round) {
-    const int settled = __syncthreads_and(t >= N || s_ptr[cur * kMaxNodes + t] == 0);
-    if (settled || round == 7) break;
-    const int nxt = cur ^ 1;
-    if (t < N) {
-      const int q = s_ptr[cur * kMaxNodes + t];
-      s_ptr[nxt * kMaxNodes + t] = s_ptr[cur * kMaxNodes + q];
-      s_dep[nxt * kMaxNodes + t] = s_dep[cur * kMaxNodes + t] + s_dep[cur * kMaxNodes + q];
-      s_acc[nxt * kMaxNodes + t] = s_acc[cur * kMaxNodes + t] & s_acc[cur * kMaxNodes + q];
+    bool mine = true;
 #pragma unroll
-      for (int w = 0; w < 4; ++w)
-        s_anc[(nxt * kMaxNodes + t) * 4 + w] = s_anc[(cur * kMaxNodes + t) * 4 + w] | s_anc[(cur * kMaxNodes + q) * 4 + w];
+    for (int sl = 0; sl < 4; ++sl) {
+      const int n = lane + 32 * sl;
+      if (n < N && s_ptr[cur * kMaxNodes + n] != 0) mine = false;
     }
+    if (__all_sync(0xffffffffu, mine) || round == 7) break;
+    const int nxt = cur ^ 1;
+#pragma unroll
+    for (int sl = 0; sl < 4; ++sl) {
+      const int n = lane + 32 * sl;
+      if (n < N) {
+        const int q = s_ptr[cur * kMaxNodes + n];
+        s_ptr[nxt * kMaxNodes + n] = s_ptr[cur * kMaxNodes + q];
+        s_dep[nxt * kMaxNodes + n] = s_dep[cur * kMaxNodes + n] + s_dep[cur * kMaxNodes + q];
+        s_acc[nxt * kMaxNodes + n] = s_acc[cur * kMaxNodes + n] & s_acc[cur * kMaxNodes + q];
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+          s_anc[(nxt * kMaxNodes + n) * 4 + w] = s_anc[(cur * kMaxNodes + n) * 4 + w] | s_anc[(cur * kMaxNodes + q) * 4 + w];
+      }
+    }
+    __syncwarp();
     cur = nxt;
   }
   // deepest accepted depth, then the nodes lying on some deepest accepted path
-  const bool acc = t < N && s_acc[cur * kMaxNodes + t] != 0u;
-  const int dep = acc ? s_dep[cur * kMaxNodes + t] : 0;
-  if (acc && dep > 0) atomicMax(s_best, dep);
-  __syncthreads();
-  const int best = *s_best;
-  if (acc && dep == best) {
+  bool acc_n[4];
+  int dep_n[4], par_n[4];
+  int best = 0;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const uint32_t a = s_anc[(cur * kMaxNodes + t) * 4 + w];
-      if (a != 0u) atomicOr(s_good + w, a);
+  for (int sl = 0; sl < 4; ++sl) {
+    const int n = lane + 32 * sl;
+    acc_n[sl] = n < N && s_acc[cur * kMaxNodes + n] != 0u;
+    dep_n[sl] = acc_n[sl] ? s_dep[cur * kMaxNodes + n] : 0;
+    par_n[sl] = n < N ? s_par[n] : -1;
+    best = max(best, dep_n[sl]);
+  }
+  best = __reduce_max_sync(0xffffffffu, best);
+  uint32_t good[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int sl = 0; sl < 4; ++sl) {
+    const int n = lane + 32 * sl;
+    if (acc_n[sl] && dep_n[sl] == best) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) good[w] |= s_anc[(cur * kMaxNodes + n) * 4 + w];
     }
   }
-  __syncthreads();
-  if (t >= 32) return;
-  // top-down (one warp): smallest-index child on a deepest path, depth by depth
-  const int lane = t;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) good[w] = __reduce_or_sync(0xffffffffu, good[w]);
+  // top-down: smallest-index child on a deepest path, depth by depth
   if (lane == 0 && best > p.max_depth) report_error(p.err, SV_DEVERR_DEPTH);
   int* out_path = p.accepted_nodes + static_cast<size_t>(b) * (p.max_depth + 1);
   int node = 0, len = best;
@@ -179,11 +200,11 @@ __device__ void walk_sequence(const Params& p, int b, int n0, int N, uint8_t* sc
   for (int d = 1; d <= best; ++d) {
     int pick = 0x7FFFFFFF;
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      const int n = lane + 32 * s;
-      const bool c = n < N && n != 0 && s_par[n] == node && ((s_good[s] >> lane) & 1u);
+    for (int sl = 0; sl < 4; ++sl) {
+      const int n = lane + 32 * sl;
+      const bool c = n < N && n != 0 && par_n[sl] == node && ((good[sl] >> lane) & 1u);
       const uint32_t bal = __ballot_sync(0xffffffffu, c);
-      if (bal != 0 && pick == 0x7FFFFFFF) pick = 32 * s + (__ffs(bal) - 1);
+      if (bal != 0 && pick == 0x7FFFFFFF) pick = 32 * sl + (__ffs(bal) - 1);
     }
     if (pick == 0x7FFFFFFF) {  // unreachable for a well-formed tree
       if (lane == 0) report_error(p.err, SV_DEVERR_BAD_TREE);
