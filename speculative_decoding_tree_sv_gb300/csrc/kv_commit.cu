@@ -45,9 +45,15 @@ __global__ void __launch_bounds__(256) kv_commit_kernel(const __grid_constant__ 
   // Launched as a programmatic dependent of the acceptance: the CTAs are
   // resident while it runs and read the accepted path once it has completed.
   griddep_wait();
+  // every index this CTA needs, requested in one round (accepted_nodes has
+  // max_depth + 1 entries per sequence, one per CTA in x, so the read is in
+  // bounds even for positions past the path)
   const int a = p.accept_len[b];
-  if (j > a) return;
   const int L = p.ctx_lens[b];
+  const int n0 = p.cu_nodes[b];
+  const int N = p.cu_nodes[b + 1] - n0;
+  const int node = p.accepted_nodes[static_cast<size_t>(b) * (p.max_depth + 1) + j];
+  if (j > a) return;
   if (a > p.max_depth) {
     // nothing of this sequence is committed, so its length stays L
     if (threadIdx.x == 0) {
@@ -57,9 +63,6 @@ __global__ void __launch_bounds__(256) kv_commit_kernel(const __grid_constant__ 
     return;
   }
   if (j == 0 && layer == 0 && threadIdx.x == 0 && p.new_ctx_lens != nullptr) p.new_ctx_lens[b] = L + a + 1;
-  const int n0 = p.cu_nodes[b];
-  const int N = p.cu_nodes[b + 1] - n0;
-  const int node = p.accepted_nodes[static_cast<size_t>(b) * (p.max_depth + 1) + j];
   if (node < 0 || node >= N) {
     if (threadIdx.x == 0) report_error(p.err, SV_DEVERR_BAD_PATH);
     return;
