@@ -145,12 +145,6 @@ __device__ __forceinline__ void tma_load_4d_mc(void* dst, const CUtensorMap* m, 
       : "memory");
 }
 
-// Orders this thread's generic-proxy shared-memory writes before later
-// async-proxy reads of them (a tcgen05.mma operand, a TMA store).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // ---------------------------------------------------------------- tcgen05
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
